@@ -1,0 +1,222 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300: forward pass of one routed sparse
+ * Mixture-of-Experts FFN layer on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer (per token t with hidden vector x_t of size D):
+ *   z_t     = x_t . Wr^T (+ bias)                       router logits over E experts
+ *   ids_t   = the k experts with the largest z_t        (exact ties: lower index)
+ *   w_t     = softmax(z_t)[ids_t] / sum of the same     renormalised gate weights
+ *   y_t     = sum_j w_tj * FFN_{ids_tj}(x_t) + FFN_shared(x_t)
+ *   FFN(x)  = W_down . (silu(W_gate . x) * (W_up . x))  SwiGLU expert
+ *
+ * Source passages (page title, section):
+ *   [P1] "Systems engineering playbook: optimizing Qwen 3.5-397B MoE on Ironwood
+ *        (TPU7x)", section 1, "Sparse Mixture-of-Experts (MoE)": router gate,
+ *        softmax over 512 experts, top-10 routed experts, always-on shared expert.
+ *   [P3] same page, section 3, "3-to-2 All-Gather optimisation": ids [T,k] and
+ *        weights [T,k] stacked on a new axis, bit-cast, one dense int32 blob.
+ *   [P3B] same page, section 3, "Option B": each device filters and computes the
+ *        inputs of its own experts (dispatch), then outputs are reduced back.
+ *   [PM] same page, executive summary: grouped GEMM and SparseCore unpermute as
+ *        reusable building blocks.
+ *   [R1] "vLLM TPU Inference v0.31.0: hierarchical MoE dispatch and W4A16",
+ *        4-bit weight section: symmetric int4 weights in the pack-quantized
+ *        format, group or channel scales, activations not quantised; weights
+ *        stay int4 in HBM and the kernel restores only the tiles it needs
+ *        on-chip; unsupported formats are rejected when the model loads.
+ *   [R1G] same page, section on dispatch shared by two cores: the EP grouped
+ *        matmul (GMM) path, with support conditions and a fallback otherwise.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers (except moe_forward_host's x and
+ *     y), row-major, contiguous, 16-byte aligned.  bf16 is IEEE bfloat16.
+ *   - The caller allocates and owns every buffer, including the workspace; the
+ *     library never allocates device memory.  Size the workspace with
+ *     moe_workspace_size() for the same entry and config.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Buffers must stay alive until the stream has passed the call.
+ *   - Concurrent calls that share a workspace race; give each stream its own.
+ *   - Return 0 on success or a negative MOE_ERR_* code.  Argument and shape
+ *     errors are detected on the host and launch nothing.  Device-side wait
+ *     timeouts are reported through moe_get_status().
+ *   - There is no fallback path: unsupported shapes return MOE_ERR_UNSUPPORTED.
+ *   - Kernels are built for sm_103a only; other devices get MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes ---- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)  /* null pointer, k < 1, k > E, T < 1, ...       */
+#define MOE_ERR_UNSUPPORTED (-2)  /* shape/format outside the kernels' envelope     */
+#define MOE_ERR_WORKSPACE (-3)    /* workspace null or smaller than required        */
+#define MOE_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed           */
+#define MOE_ERR_TIMEOUT (-5)      /* a device wait hit its bound (moe_get_status)   */
+#define MOE_ERR_ALIGN (-6)        /* a pointer is not 16-byte aligned               */
+
+/* ---- weight formats ---- */
+#define MOE_QUANT_BF16 0    /* bf16 expert weights                                   */
+#define MOE_QUANT_W4A16 1   /* symmetric int4, 8 per int32 (value j in bits 4j..4j+3,
+                               two's complement), bf16 scale per `group` K values [R1] */
+
+/* ---- grouped GEMM operations ---- */
+#define MOE_OP_GATE_UP_SWIGLU 0  /* h = silu(a.Wg^T) * (a.Wu^T) -> bf16               */
+#define MOE_OP_DOWN_WEIGHTED 1   /* o = w_row * (h.Wd^T)      -> fp32                 */
+
+/* ---- entries (for moe_workspace_size) ---- */
+#define MOE_ENTRY_ROUTE 0
+#define MOE_ENTRY_PERMUTE 1
+#define MOE_ENTRY_GROUPED_GEMM 2
+#define MOE_ENTRY_FORWARD 3
+#define MOE_ENTRY_FORWARD_HOST 4
+
+/*
+ * Shapes of one layer call.
+ *   T        tokens (1 .. 2^20), D hidden size (multiple of 128),
+ *   E        routed experts (1 .. 1024), I / I_shared expert intermediate sizes
+ *            (multiples of 64; of `group` for W4A16), k experts per token
+ *            (1 .. min(E, 32)), quant MOE_QUANT_*, group = 128 for W4A16.
+ */
+typedef struct moe_config {
+  int T, D, E, I, I_shared, k;
+  int quant;
+  int group;
+} moe_config;
+
+/*
+ * Layer weights (device pointers).  Gate/up of an expert is one [2I][D]
+ * matrix with the I gate rows first; down is [D][I].  Both are K-major:
+ * rows are output features [P1, reading of the expert form].
+ *   quant == BF16 : w_gate_up bf16 [E][2I][D], w_down bf16 [E][D][I];
+ *                   scale pointers must be NULL.
+ *   quant == W4A16: w_gate_up int32 [E][2I][D/8] + s_gate_up bf16 [E][2I][D/group],
+ *                   w_down int32 [E][D][I/8] + s_down bf16 [E][D][I/group].
+ *   The shared expert (ws_*, ss_*) has the same format with I_shared and no
+ *   leading E.  w_router is bf16 [E][D] in both cases; router_bias is fp32 [E]
+ *   or NULL.
+ */
+typedef struct moe_weights {
+  const void *w_router;
+  const float *router_bias;
+  const void *w_gate_up, *w_down, *s_gate_up, *s_down;
+  const void *ws_gate_up, *ws_down, *ss_gate_up, *ss_down;
+} moe_weights;
+
+/*
+ * Arguments of one grouped GEMM over the E routed experts, plus an optional
+ * shared-expert group covering all T tokens with weight 1 [P1, PM, R1G].
+ * Routed group e owns GEMM rows [offsets[e], offsets[e+1]).
+ *   op == GATE_UP_SWIGLU:
+ *     a      bf16 [rows][D]; row r of the GEMM reads a[r], or a[a_row_index[r]]
+ *            when a_row_index is non-NULL (then `a` is [T][D] and a_row_index
+ *            holds token indices; the rows are gathered into the workspace);
+ *     w      expert gate/up weights (format per cfg->quant), w_scales or NULL;
+ *     out    bf16 [P][I]: h = silu(a.Wg^T) * (a.Wu^T), rounded once to bf16.
+ *     a_shared bf16 [T][D] (NULL: no shared group), w_shared/ws_scales the
+ *            shared gate/up weights, out_shared bf16 [T][I_shared].
+ *   op == DOWN_WEIGHTED:
+ *     a      bf16 [P][I] (a_row_index must be NULL);
+ *     w      expert down weights; out fp32 [P][D] = wgt(r) * (a_r . Wd^T),
+ *            wgt(r) = the blob weight of pair perm_pair[r] (t = p/k, j = p%k).
+ *     a_shared bf16 [T][I_shared], w_shared [D][I_shared], out_shared fp32 [T][D]
+ *            (weight 1).
+ */
+typedef struct moe_gemm_args {
+  int op;
+  const void *a;
+  const int32_t *a_row_index;
+  const int32_t *offsets;
+  const void *w, *w_scales;
+  const int32_t *perm_pair;
+  const int32_t *blob;
+  void *out;
+  const void *a_shared;
+  const void *w_shared, *ws_scales;
+  void *out_shared;
+} moe_gemm_args;
+
+/*
+ * Workspace bytes an entry needs for `cfg` (0 on invalid config).  The first
+ * 256 bytes of every workspace are a status header read by moe_get_status.
+ */
+size_t moe_workspace_size(const moe_config *cfg, int entry);
+
+/*
+ * Router [P1, P3]: logits z = x.Wr^T + bias, top-k by (logit desc, index asc),
+ * softmax over all E then renormalised over the k selected, packed into
+ *   blob int32 [T][2][k]: blob[t][0][j] = expert id (ascending in j),
+ *                         blob[t][1][j] = fp32 bit pattern of its weight.
+ * The selected set equals the one decided by fp64 index-order logits: fp32
+ * logits carry a rigorous error radius, and tokens whose boundary is not
+ * certified are re-decided in fp64.
+ *   x bf16 [T][D], w_router bf16 [E][D], bias fp32 [E] or NULL.
+ */
+int moe_route(const moe_config *cfg, const void *x, const void *w_router,
+              const float *bias, int32_t *blob, void *ws, size_t ws_bytes,
+              void *stream);
+
+/*
+ * Dispatch [P3B]: group the T*k (token, slot) pairs by expert, stable in the
+ * pair index p = t*k + j.
+ *   counts int32 [E], offsets int32 [E+1] (exclusive scan; offsets[E] = T*k),
+ *   perm_pair int32 [T*k]: grouped row r holds pair perm_pair[r],
+ *   inv_row int32 [T*k]:   pair p sits in grouped row inv_row[p].
+ * Bit-exact and deterministic.  Expert ids outside [0, E) are undefined input.
+ */
+int moe_permute(const moe_config *cfg, const int32_t *blob, int32_t *counts,
+                int32_t *offsets, int32_t *perm_pair, int32_t *inv_row,
+                void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Persistent grouped GEMM over ragged expert row groups (TMA + tcgen05/TMEM)
+ * [PM, R1G, R1]; see moe_gemm_args for operands.  W4A16 weights are
+ * dequantised tile by tile in shared memory just ahead of the MMA [R1].
+ */
+int moe_grouped_gemm(const moe_config *cfg, const moe_gemm_args *args, void *ws,
+                     size_t ws_bytes, void *stream);
+
+/*
+ * Combine / unpermute [PM, P3B]:
+ *   y[t][d] = bf16_rne( o_shared[t][d] + sum_j o[inv_row[t*k+j]][d] )
+ * with o fp32 [T*k][D] already weighted, o_shared fp32 [T][D] or NULL, y bf16 [T][D].
+ */
+int moe_combine(const moe_config *cfg, const float *o, const float *o_shared,
+                const int32_t *inv_row, void *y, void *stream);
+
+/*
+ * Whole layer: route -> permute -> grouped gate/up (+shared) -> grouped down
+ * (+shared) -> combine.  x bf16 [T][D], y bf16 [T][D].
+ */
+int moe_forward(const moe_config *cfg, const void *x, const moe_weights *w,
+                void *y, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_forward with HOST x and y (pinned memory recommended): copies x into the
+ * workspace, runs the layer, copies y back, all on `stream`.  The caller
+ * synchronises the stream before reading y.
+ */
+int moe_forward_host(const moe_config *cfg, const void *x_host,
+                     const moe_weights *w, void *y_host, void *ws,
+                     size_t ws_bytes, void *stream);
+
+/*
+ * Device status of the last calls that used `ws`: synchronises `stream`,
+ * returns MOE_OK or the first device-side error recorded (MOE_ERR_TIMEOUT
+ * when a bounded wait inside a kernel gave up), then clears it.
+ */
+int moe_get_status(void *ws, void *stream);
+
+/* Static description of an error code. */
+const char *moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -63,6 +63,12 @@ def _load():
             lib.oracle_dequant_w4.argtypes = [I, I, I, P, P, P]
             lib.oracle_forward.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_expert_hidden.argtypes = [I, I, I, I, I, P, P, P, P]
+            lib.oracle_expert_down.argtypes = [I, I, I, I, I, P, P, P, P]
+            lib.oracle_expert_hidden.restype = ctypes.c_int
+            lib.oracle_combine.argtypes = [I, I, I, P, P, P, P]
+            lib.oracle_combine.restype = ctypes.c_int
+            lib.oracle_expert_down.restype = ctypes.c_int
             for f in (lib.oracle_router_logits, lib.oracle_route, lib.oracle_pack_blob,
                       lib.oracle_unpack_blob, lib.oracle_permute, lib.oracle_dequant_w4,
                       lib.oracle_forward, lib.oracle_num_threads):
@@ -159,6 +165,46 @@ def dequant_w4(q, s, group):
     out = np.empty((R, C), np.float64)
     _check(_load().oracle_dequant_w4(R, C, group, _ptr(q), _ptr(s), _ptr(out)), "dequant_w4")
     return out
+
+
+def expert_hidden(x_rows, w_gate_up, s_gate_up=None, *, group=128):
+    """SwiGLU hidden (fp64) of one expert for each row: [n, Ie]."""
+    x_rows = _c(x_rows, np.uint16)
+    n, D = x_rows.shape
+    quant = 0 if s_gate_up is None else 1
+    wg = _c(w_gate_up, np.uint16 if quant == 0 else np.int32)
+    sg = None if quant == 0 else _c(s_gate_up, np.uint16)
+    Ie = wg.shape[0] // 2
+    h = np.empty((n, Ie), np.float64)
+    _check(_load().oracle_expert_hidden(n, D, Ie, quant, group, _ptr(x_rows), _ptr(wg), _ptr(sg),
+                                        _ptr(h)), "expert_hidden")
+    return h
+
+
+def expert_down(h, w_down, s_down=None, *, group=128):
+    """Down projection (fp64) of one expert for each row of h [n, Ie]: [n, D]."""
+    h = _c(h, np.float64)
+    n, Ie = h.shape
+    quant = 0 if s_down is None else 1
+    wd = _c(w_down, np.uint16 if quant == 0 else np.int32)
+    sd = None if quant == 0 else _c(s_down, np.uint16)
+    D = wd.shape[0]
+    o = np.empty((n, D), np.float64)
+    _check(_load().oracle_expert_down(n, D, Ie, quant, group, _ptr(h), _ptr(wd), _ptr(sd), _ptr(o)),
+           "expert_down")
+    return o
+
+
+def combine(o, o_shared, inv_row, k):
+    """y [T, D] (fp64) = o_shared[t] + sum_j o[inv_row[t*k+j]]."""
+    o = _c(o, np.float64)
+    inv_row = _c(inv_row, np.int32).reshape(-1)
+    T = inv_row.size // k
+    D = o.shape[1]
+    osh = None if o_shared is None else _c(o_shared, np.float64)
+    y = np.empty((T, D), np.float64)
+    _check(_load().oracle_combine(T, D, k, _ptr(o), _ptr(osh), _ptr(inv_row), _ptr(y)), "combine")
+    return y
 
 
 def forward(x_rows, ids, w, experts, shared, *, E, I, Is, quant=0, group=128):

@@ -374,6 +374,89 @@ int oracle_forward(int nt, int D, int E, int I, int Is, int k, int quant,
   return err;
 }
 
+/* ------------------------------------------------------------------ */
+/* The two halves of one expert, exposed for per-kernel checks:         */
+/*   oracle_expert_hidden:  h[n][i] = silu(<Wgu[i], x_n>) * <Wgu[I+i], x_n> */
+/*   oracle_expert_down:    o[n][c] = <Wdn[c], h_n>                     */
+/* Weight formats as in oracle_forward (quant 0: bf16; 1: int4 + scales). */
+/* ------------------------------------------------------------------ */
+int oracle_expert_hidden(int n, int D, int Ie, int quant, int group,
+                         const uint16_t *x, const void *w_gu, const uint16_t *s_gu,
+                         double *h) {
+  if (n < 0 || D < 1 || Ie < 1 || !x || !w_gu || !h) return ORACLE_EINVAL;
+  if (quant == 1 && (!s_gu || group < 1 || D % group || D % 8)) return ORACLE_EINVAL;
+  wview gu = {2 * Ie, D, quant, group, NULL, NULL, NULL};
+  if (quant == 0) gu.bf16 = (const uint16_t *)w_gu;
+  else { gu.q = (const int32_t *)w_gu; gu.s = s_gu; }
+  int err = ORACLE_OK;
+#pragma omp parallel
+  {
+    double *xd = (double *)malloc(sizeof(double) * (size_t)D);
+    double *row = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!xd || !row) {
+#pragma omp atomic write
+      err = ORACLE_ENOMEM;
+    } else {
+#pragma omp for schedule(static)
+      for (int r = 0; r < n; ++r) {
+        for (int d = 0; d < D; ++d) xd[d] = bf16_to_f64(x[(size_t)r * D + d]);
+        for (int i = 0; i < Ie; ++i) {
+          load_row(&gu, i, row);
+          double g = dot(row, xd, D);
+          load_row(&gu, Ie + i, row);
+          double u = dot(row, xd, D);
+          h[(size_t)r * Ie + i] = silu(g) * u;
+        }
+      }
+    }
+    free(xd);
+    free(row);
+  }
+  return err;
+}
+
+int oracle_expert_down(int n, int D, int Ie, int quant, int group, const double *h,
+                       const void *w_dn, const uint16_t *s_dn, double *o) {
+  if (n < 0 || D < 1 || Ie < 1 || !h || !w_dn || !o) return ORACLE_EINVAL;
+  if (quant == 1 && (!s_dn || group < 1 || Ie % group || Ie % 8)) return ORACLE_EINVAL;
+  wview dn = {D, Ie, quant, group, NULL, NULL, NULL};
+  if (quant == 0) dn.bf16 = (const uint16_t *)w_dn;
+  else { dn.q = (const int32_t *)w_dn; dn.s = s_dn; }
+  int err = ORACLE_OK;
+#pragma omp parallel
+  {
+    double *row = (double *)malloc(sizeof(double) * (size_t)Ie);
+    if (!row) {
+#pragma omp atomic write
+      err = ORACLE_ENOMEM;
+    } else {
+#pragma omp for schedule(static)
+      for (int c = 0; c < D; ++c) {
+        load_row(&dn, c, row);
+        for (int r = 0; r < n; ++r) o[(size_t)r * D + c] = dot(row, h + (size_t)r * Ie, Ie);
+      }
+    }
+    free(row);
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------ */
+/* Unpermute + combine: y[t][d] = o_shared[t][d] + sum_j o[inv_row[t*k+j]][d] */
+/* (o already weighted; o_shared may be NULL).                          */
+/* ------------------------------------------------------------------ */
+int oracle_combine(int T, int D, int k, const double *o, const double *o_shared,
+                   const int32_t *inv_row, double *y) {
+  if (T < 0 || D < 1 || k < 1 || !o || !inv_row || !y) return ORACLE_EINVAL;
+  for (int t = 0; t < T; ++t)
+    for (int d = 0; d < D; ++d) {
+      double acc = o_shared ? o_shared[(size_t)t * D + d] : 0.0;
+      for (int j = 0; j < k; ++j) acc += o[(size_t)inv_row[(size_t)t * k + j] * D + d];
+      y[(size_t)t * D + d] = acc;
+    }
+  return ORACLE_OK;
+}
+
 /* Threads OpenMP will use (reported beside CPU timings). */
 int oracle_num_threads(void) {
   int n = 1;

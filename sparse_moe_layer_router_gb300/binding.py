@@ -1,0 +1,224 @@
+"""ctypes binding of the libmoe_gb300 C ABI (``include/moe.h``).
+
+Argument marshalling only: torch tensors become device pointers, the current
+torch CUDA stream becomes the ``stream`` argument, and a negative return code
+becomes ``MoeError``.  Every step of the layer runs in the library's kernels.
+There is no fallback: a missing library or a missing GPU raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_WORKSPACE = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_TIMEOUT = -5
+MOE_ERR_ALIGN = -6
+
+MOE_QUANT_BF16 = 0
+MOE_QUANT_W4A16 = 1
+MOE_OP_GATE_UP_SWIGLU = 0
+MOE_OP_DOWN_WEIGHTED = 1
+MOE_ENTRY_ROUTE = 0
+MOE_ENTRY_PERMUTE = 1
+MOE_ENTRY_GROUPED_GEMM = 2
+MOE_ENTRY_FORWARD = 3
+MOE_ENTRY_FORWARD_HOST = 4
+
+# Every function declared in include/moe.h.
+EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_gemm", "moe_combine",
+           "moe_forward", "moe_forward_host", "moe_get_status", "moe_strerror")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("D", ctypes.c_int), ("E", ctypes.c_int), ("I", ctypes.c_int),
+                ("I_shared", ctypes.c_int), ("k", ctypes.c_int), ("quant", ctypes.c_int),
+                ("group", ctypes.c_int)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w_router", "router_bias", "w_gate_up", "w_down", "s_gate_up", "s_down", "ws_gate_up",
+        "ws_down", "ss_gate_up", "ss_down")]
+
+
+class MoeGemmArgs(ctypes.Structure):
+    _fields_ = [("op", ctypes.c_int)] + [(n, ctypes.c_void_p) for n in (
+        "a", "a_row_index", "offsets", "w", "w_scales", "perm_pair", "blob", "out", "a_shared",
+        "w_shared", "ws_scales", "out_shared")]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load libmoe_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m sparse_moe_layer_router_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            cfgp = ctypes.POINTER(MoeConfig)
+            L.moe_workspace_size.argtypes = [cfgp, I]
+            L.moe_workspace_size.restype = S
+            L.moe_route.argtypes = [cfgp, P, P, P, P, P, S, P]
+            L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, S, P]
+            L.moe_grouped_gemm.argtypes = [cfgp, ctypes.POINTER(MoeGemmArgs), P, S, P]
+            L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
+            L.moe_forward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
+            L.moe_forward_host.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
+            L.moe_get_status.argtypes = [P, P]
+            L.moe_strerror.argtypes = [I]
+            L.moe_strerror.restype = ctypes.c_char_p
+            for n in ("moe_route", "moe_permute", "moe_grouped_gemm", "moe_combine", "moe_forward",
+                      "moe_forward_host", "moe_get_status"):
+                getattr(L, n).restype = I
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().moe_strerror(int(code)).decode()
+
+
+def config(cfg) -> MoeConfig:
+    """MoeConfig from any object with T, D, E, I, Is, k, quant, group attributes."""
+    return MoeConfig(cfg.T, cfg.D, cfg.E, cfg.I, cfg.Is, cfg.k, cfg.quant, cfg.group)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return ctypes.c_void_p(int(t))
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+def workspace_size(cfg, entry: int) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(config(cfg)), entry))
+
+
+def workspace(cfg, entry: int, device=None) -> torch.Tensor:
+    n = workspace_size(cfg, entry)
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    ws[:256].zero_()
+    return ws
+
+
+def route(cfg, x, w_router, bias=None, blob=None, ws=None, stream=None):
+    """int32 blob [T, 2, k] (ids ascending, then fp32 weight bits)."""
+    if blob is None:
+        blob = torch.empty((cfg.T, 2, cfg.k), dtype=torch.int32, device=x.device)
+    if ws is None:
+        ws = workspace(cfg, MOE_ENTRY_ROUTE, x.device)
+    _check(lib().moe_route(ctypes.byref(config(cfg)), _p(x), _p(w_router), _p(bias), _p(blob),
+                           _p(ws), ws.numel(), _stream(stream)), "moe_route")
+    return blob
+
+
+def permute(cfg, blob, ws=None, stream=None):
+    """(counts [E], offsets [E+1], perm_pair [T*k], inv_row [T*k]) int32."""
+    dev = blob.device
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
+    inv = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(cfg, MOE_ENTRY_PERMUTE, dev)
+    _check(lib().moe_permute(ctypes.byref(config(cfg)), _p(blob), _p(counts), _p(offsets), _p(perm),
+                             _p(inv), _p(ws), ws.numel(), _stream(stream)), "moe_permute")
+    return counts, offsets, perm, inv
+
+
+def grouped_gemm(cfg, op, a, offsets, w, out, *, a_row_index=None, w_scales=None, perm_pair=None,
+                 blob=None, a_shared=None, w_shared=None, ws_scales=None, out_shared=None,
+                 ws=None, stream=None):
+    """One grouped GEMM launch (see moe_gemm_args in include/moe.h)."""
+    args = MoeGemmArgs(op, _p(a), _p(a_row_index), _p(offsets), _p(w), _p(w_scales),
+                       _p(perm_pair), _p(blob), _p(out), _p(a_shared), _p(w_shared),
+                       _p(ws_scales), _p(out_shared))
+    if ws is None:
+        ws = workspace(cfg, MOE_ENTRY_GROUPED_GEMM, a.device)
+    _check(lib().moe_grouped_gemm(ctypes.byref(config(cfg)), ctypes.byref(args), _p(ws), ws.numel(),
+                                  _stream(stream)), "moe_grouped_gemm")
+    return out, out_shared
+
+
+def combine(cfg, o, o_shared, inv_row, y=None, stream=None):
+    if y is None:
+        y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=o.device)
+    _check(lib().moe_combine(ctypes.byref(config(cfg)), _p(o), _p(o_shared), _p(inv_row), _p(y),
+                             _stream(stream)), "moe_combine")
+    return y
+
+
+def weights_struct(inp) -> MoeWeights:
+    """MoeWeights from a MoEInputs (all tensors on the GPU)."""
+    return MoeWeights(_p(inp.w_router), _p(inp.bias), _p(inp.w_gate_up), _p(inp.w_down),
+                      _p(inp.s_gate_up), _p(inp.s_down), _p(inp.ws_gate_up), _p(inp.ws_down),
+                      _p(inp.ss_gate_up), _p(inp.ss_down))
+
+
+def forward(cfg, x, weights, y=None, ws=None, stream=None):
+    """Whole layer; ``weights`` is a MoeWeights or a MoEInputs on the GPU."""
+    if not isinstance(weights, MoeWeights):
+        weights = weights_struct(weights)
+    if y is None:
+        y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(cfg, MOE_ENTRY_FORWARD, x.device)
+    _check(lib().moe_forward(ctypes.byref(config(cfg)), _p(x), ctypes.byref(weights), _p(y), _p(ws),
+                             ws.numel(), _stream(stream)), "moe_forward")
+    return y
+
+
+def forward_host(cfg, x_host, weights, y_host, ws, stream=None):
+    """Whole layer with host x / y (pinned CPU tensors); caller synchronises."""
+    if not isinstance(weights, MoeWeights):
+        weights = weights_struct(weights)
+    for t in (x_host, y_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("forward_host takes contiguous CPU tensors")
+    _check(lib().moe_forward_host(ctypes.byref(config(cfg)), ctypes.c_void_p(x_host.data_ptr()),
+                                  ctypes.byref(weights), ctypes.c_void_p(y_host.data_ptr()),
+                                  _p(ws), ws.numel(), _stream(stream)), "moe_forward_host")
+    return y_host
+
+
+def get_status(ws, stream=None) -> int:
+    return int(lib().moe_get_status(_p(ws), _stream(stream)))

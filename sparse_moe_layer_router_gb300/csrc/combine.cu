@@ -1,0 +1,51 @@
+// combine.cu -- unpermute and sum the weighted expert outputs into token order.
+//
+// "Systems engineering playbook: optimizing Qwen 3.5-397B MoE on Ironwood
+// (TPU7x)": the reusable "SparseCore unpermute" block (executive summary) and
+// section 3 "Option B" (expert outputs are reduced back to their tokens);
+// section 1 "Sparse Mixture-of-Experts (MoE)": the shared expert is added.
+//
+//   y[t][d] = bf16_rne( o_shared[t][d] + sum_{j<k} o[inv_row[t*k+j]][d] )
+//
+// fp32 sum in that fixed order, then one rounding.  HBM-bound: each thread
+// moves 4 consecutive fp32 per source row (16-byte loads), 8 bytes of output.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ o,
+                                                      const float4* __restrict__ o_shared,
+                                                      const int32_t* __restrict__ inv_row, int T,
+                                                      int D4, int k, uint2* __restrict__ y) {
+  const int t = blockIdx.x;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c >= D4) return;
+  float4 acc = o_shared ? __ldg(o_shared + static_cast<size_t>(t) * D4 + c)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int32_t* rows = inv_row + static_cast<size_t>(t) * k;
+  for (int j = 0; j < k; ++j) {
+    const float4 v = __ldg(o + static_cast<size_t>(__ldg(rows + j)) * D4 + c);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 out;
+  out.x = *reinterpret_cast<const uint32_t*>(&lo);
+  out.y = *reinterpret_cast<const uint32_t*>(&hi);
+  y[static_cast<size_t>(t) * D4 + c] = out;
+}
+
+void launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T, int D,
+                    int k, void* y, cudaStream_t st) {
+  const int D4 = D / 4;
+  dim3 grid(T, (D4 + 255) / 256);
+  combine_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(o),
+                                       reinterpret_cast<const float4*>(o_shared), inv_row, T, D4,
+                                       k, static_cast<uint2*>(y));
+}
+
+}  // namespace moe

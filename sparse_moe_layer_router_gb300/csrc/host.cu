@@ -1,0 +1,521 @@
+// host.cu -- the C ABI of libmoe_gb300 (declared in include/moe.h).
+//
+// Validates shapes and pointers on the host (nothing is launched on an
+// error), lays out the caller's workspace, encodes TMA tensor maps and
+// launches the kernels on the caller's stream.  The library allocates no
+// device memory and keeps no state besides per-device constants.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace moe;
+
+constexpr size_t kHeader = 256;  // status word (int32 at 0), refine counter (int32 at 4)
+constexpr int kRouterTargetCtas = 304;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- devices
+struct DevInfo {
+  int checked = 0;
+  int ok = 0;
+  int sms = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+int current_device(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.ok = (major == 10 && minor == 3);
+    d.sms = sms;
+    d.checked = 1;
+  }
+  if (!d.ok) return MOE_ERR_UNSUPPORTED;
+  *out = d;
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Row-major bf16 matrix [rows][cols] as a 2-D map with a {64, box_rows} box, 128-B swizzle.
+bool map_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Gate/up weights [groups][2*half][cols]: 3-D map {cols, groups*2*half rows, 2} whose
+// third axis steps from a gate row to the matching up row (half rows further);
+// box {64, 16, 2} = 16 gate rows followed by the 16 matching up rows.
+bool map_gate_up_bf16(CUtensorMap* m, const void* base, uint64_t groups, uint64_t half,
+                      uint64_t cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {cols, groups * 2 * half, 2};
+  const cuuint64_t strides[2] = {cols * 2, half * cols * 2};
+  const cuuint32_t box[3] = {64, 16, 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- validation
+int validate(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->D < 1 || c->E < 1 || c->I < 1 || c->I_shared < 1 || c->k < 1 || c->k > c->E)
+    return MOE_ERR_INVALID_ARG;
+  if (c->T > (1 << 20) || c->E > 1024 || c->k > 32) return MOE_ERR_UNSUPPORTED;
+  if (c->D % 128 != 0 || c->D > 65536) return MOE_ERR_UNSUPPORTED;
+  if (c->I > 65536 || c->I_shared > 65536) return MOE_ERR_UNSUPPORTED;
+  if (c->quant == MOE_QUANT_BF16) {
+    if (c->I % 64 != 0 || c->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  } else if (c->quant == MOE_QUANT_W4A16) {
+    // symmetric int4, group 128 along K only (other layouts are rejected, as
+    // unsupported quantisation formats are rejected at model load)
+    if (c->group != 128 || c->I % 128 != 0 || c->I_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  } else {
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------- workspace
+struct RouterPlan {
+  int S = 1;
+  int sub_per_split = 1;
+};
+
+RouterPlan router_plan(const moe_config* c) {
+  RouterPlan r;
+  const int nsub = c->D / 64;
+  const long base = static_cast<long>((c->E + 63) / 64) * ((c->T + 63) / 64);
+  long S = (kRouterTargetCtas + base - 1) / base;
+  if (S > 16) S = 16;
+  if (S > nsub) S = nsub;
+  if (S < 1) S = 1;
+  r.sub_per_split = (nsub + static_cast<int>(S) - 1) / static_cast<int>(S);
+  r.S = (nsub + r.sub_per_split - 1) / r.sub_per_split;
+  return r;
+}
+
+struct Layout {
+  size_t blob = 0, zpart = 0, xnorm = 0, wnorm = 0;            // route
+  size_t chunk = 0;                                              // permute
+  size_t counts = 0, offsets = 0, perm = 0, inv = 0;             // forward
+  size_t xperm = 0, h = 0, hs = 0, o = 0, os = 0, xin = 0, yout = 0;
+  size_t total = 0;
+};
+
+struct Carver {
+  size_t cur = kHeader;
+  size_t take(size_t bytes) {
+    const size_t at = cur;
+    cur = align_up(cur + bytes, 256);
+    return at;
+  }
+};
+
+Layout layout(const moe_config* c, int entry) {
+  Layout L;
+  Carver cv;
+  const size_t T = c->T, D = c->D, E = c->E, k = c->k, P = T * k;
+  const size_t I = c->I, Is = c->I_shared;
+  const RouterPlan rp = router_plan(c);
+  const size_t chunks = (P + kPermuteChunk - 1) / kPermuteChunk;
+  auto route_part = [&] {
+    L.zpart = cv.take(static_cast<size_t>(rp.S) * T * E * 4);
+    L.xnorm = cv.take(T * 4);
+    L.wnorm = cv.take(E * 4);
+  };
+  switch (entry) {
+    case MOE_ENTRY_ROUTE:
+      route_part();
+      break;
+    case MOE_ENTRY_PERMUTE:
+      L.chunk = cv.take(chunks * E * 4);
+      break;
+    case MOE_ENTRY_GROUPED_GEMM:
+      L.xperm = cv.take(P * D * 2);  // gathered activation rows when a_row_index is given
+      break;
+    case MOE_ENTRY_FORWARD:
+    case MOE_ENTRY_FORWARD_HOST:
+      L.blob = cv.take(T * 2 * k * 4);
+      route_part();
+      L.chunk = cv.take(chunks * E * 4);
+      L.counts = cv.take(E * 4);
+      L.offsets = cv.take((E + 1) * 4);
+      L.perm = cv.take(P * 4);
+      L.inv = cv.take(P * 4);
+      L.xperm = cv.take(P * D * 2);
+      L.h = cv.take(P * I * 2);
+      L.hs = cv.take(T * Is * 2);
+      L.o = cv.take(P * D * 4);
+      L.os = cv.take(T * D * 4);
+      if (entry == MOE_ENTRY_FORWARD_HOST) {
+        L.xin = cv.take(T * D * 2);
+        L.yout = cv.take(T * D * 2);
+      }
+      break;
+    default:
+      return L;
+  }
+  L.total = cv.cur;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Error radius factor of the fp32 router logits (see router.cu): products pass
+// through at most h = 64 + sub_per_split + S + 2 fp32 roundings; the fp64
+// index-order definition deviates from the exact sum by at most D * 2^-53
+// relative to sum |x_d w_d|.
+float router_gamma(const moe_config* c, const RouterPlan& rp) {
+  const double u = std::ldexp(1.0, -24);
+  const double h = 64.0 + rp.sub_per_split + rp.S + 2.0;
+  const double g = h * u / (1.0 - h * u) + c->D * std::ldexp(1.0, -53) * 1.01;
+  return std::nextafter(static_cast<float>(g), INFINITY);
+}
+
+int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* wr,
+               const float* bias, int32_t* blob, void* ws, const Layout& L, cudaStream_t st) {
+  const RouterPlan rp = router_plan(c);
+  // Clears the status word and the refine counter for this call.
+  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
+  float* zpart = at<float>(ws, L.zpart);
+  float* xn = at<float>(ws, L.xnorm);
+  float* wn = at<float>(ws, L.wnorm);
+  launch_row_norms(x, c->T, c->D, xn, st);
+  launch_row_norms(wr, c->E, c->D, wn, st);
+  launch_router_logits(x, wr, c->T, c->D, c->E, rp.S, rp.sub_per_split, zpart, st);
+  return cuda_rc(launch_router_select(zpart, rp.S, c->T, c->D, c->E, c->k, bias, xn, wn,
+                                      router_gamma(c, rp), x, wr, blob, at<int>(ws, 4), st));
+}
+
+int choose_bn_max(const moe_config* c) {
+  const double avg = static_cast<double>(c->T) * c->k / c->E;
+  return (c->T >= 2048 || avg >= 48.0) ? 256 : 64;
+}
+
+int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, void* ws,
+              const Layout& L, cudaStream_t st, void* xperm_override) {
+  const int P = c->T * c->k;
+  const bool gate_up = a->op == MOE_OP_GATE_UP_SWIGLU;
+  const bool has_shared = a->a_shared != nullptr;
+  if (c->quant != MOE_QUANT_BF16) return MOE_ERR_UNSUPPORTED;
+  const void* b_routed = a->a;
+  if (a->a_row_index) {
+    if (!gate_up) return MOE_ERR_INVALID_ARG;
+    void* xp = xperm_override ? xperm_override : at<void>(ws, L.xperm);
+    launch_gather_rows(a->a, a->a_row_index, P, c->D, 1, xp, st);
+    b_routed = xp;
+  }
+  GemmMaps maps;
+  GemmParams p{};
+  p.op = gate_up ? kOpGateUp : kOpDown;
+  p.E = c->E;
+  p.has_shared = has_shared ? 1 : 0;
+  p.T_shared = c->T;
+  p.offsets = a->offsets;
+  p.perm_pair = a->perm_pair;
+  p.blob = a->blob;
+  p.k = c->k;
+  p.status = at<int>(ws, 0);
+  p.out = a->out;
+  p.out_s = a->out_shared;
+  bool ok = true;
+  if (gate_up) {
+    p.m_tiles = c->I / 64;
+    p.m_tiles_s = c->I_shared / 64;
+    p.k_blocks = p.k_blocks_s = c->D / 64;
+    p.a_rows_per_expert = 2 * c->I;
+    p.ld_out = c->I;
+    p.ld_out_s = c->I_shared;
+    ok &= map_gate_up_bf16(&maps.a, a->w, c->E, c->I, c->D);
+    ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, 16);
+    if (has_shared) {
+      ok &= map_gate_up_bf16(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
+      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->D, 16);
+    }
+  } else {
+    p.m_tiles = c->D / 128;
+    p.m_tiles_s = c->D / 128;
+    p.k_blocks = c->I / 64;
+    p.k_blocks_s = c->I_shared / 64;
+    p.a_rows_per_expert = c->D;
+    p.ld_out = c->D;
+    p.ld_out_s = c->D;
+    ok &= map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128);
+    ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, 16);
+    if (has_shared) {
+      ok &= map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
+      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, 16);
+    }
+  }
+  if (!ok) return MOE_ERR_CUDA;
+  if (!has_shared) {
+    maps.a_s = maps.a;
+    maps.b_s = maps.b;
+  }
+  return cuda_rc(launch_grouped_gemm(p, maps, choose_bn_max(c), c->quant, dev.sms, st));
+}
+
+int check_gemm_args(const moe_config* c, const moe_gemm_args* a) {
+  if (!a || !a->a || !a->offsets || !a->w || !a->out) return MOE_ERR_INVALID_ARG;
+  if (a->op != MOE_OP_GATE_UP_SWIGLU && a->op != MOE_OP_DOWN_WEIGHTED) return MOE_ERR_INVALID_ARG;
+  if (a->op == MOE_OP_DOWN_WEIGHTED && (!a->perm_pair || !a->blob)) return MOE_ERR_INVALID_ARG;
+  if (a->a_shared && (!a->w_shared || !a->out_shared)) return MOE_ERR_INVALID_ARG;
+  if (c->quant == MOE_QUANT_W4A16 && (!a->w_scales || (a->a_shared && !a->ws_scales)))
+    return MOE_ERR_INVALID_ARG;
+  if (c->quant == MOE_QUANT_BF16 && (a->w_scales || a->ws_scales)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->a, a->w, a->w_scales, a->out, a->a_shared, a->w_shared, a->ws_scales,
+                        a->out_shared, a->offsets};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+int check_weights(const moe_config* c, const moe_weights* w) {
+  if (!w || !w->w_router || !w->w_gate_up || !w->w_down || !w->ws_gate_up || !w->ws_down)
+    return MOE_ERR_INVALID_ARG;
+  if (c->quant == MOE_QUANT_W4A16 &&
+      (!w->s_gate_up || !w->s_down || !w->ss_gate_up || !w->ss_down))
+    return MOE_ERR_INVALID_ARG;
+  if (c->quant == MOE_QUANT_BF16 && (w->s_gate_up || w->s_down || w->ss_gate_up || w->ss_down))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->w_router, w->w_gate_up, w->w_down, w->s_gate_up, w->s_down,
+                        w->ws_gate_up, w->ws_down, w->ss_gate_up, w->ss_down};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const moe_weights* w,
+                 void* y, void* ws, const Layout& L, cudaStream_t st) {
+  int rc = route_impl(c, dev, x, w->w_router, w->router_bias, at<int32_t>(ws, L.blob), ws, L, st);
+  if (rc) return rc;
+  rc = cuda_rc(launch_permute(at<int32_t>(ws, L.blob), c->T, c->k, c->E, at<int32_t>(ws, L.chunk),
+                              at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                              at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), st));
+  if (rc) return rc;
+  // dispatch: token rows in grouped order (pair index / k = token)
+  launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k, at<void>(ws, L.xperm),
+                     st);
+  moe_gemm_args g{};
+  g.op = MOE_OP_GATE_UP_SWIGLU;
+  g.a = at<void>(ws, L.xperm);
+  g.offsets = at<int32_t>(ws, L.offsets);
+  g.w = w->w_gate_up;
+  g.w_scales = w->s_gate_up;
+  g.out = at<void>(ws, L.h);
+  g.a_shared = x;
+  g.w_shared = w->ws_gate_up;
+  g.ws_scales = w->ss_gate_up;
+  g.out_shared = at<void>(ws, L.hs);
+  rc = gemm_impl(c, dev, &g, ws, L, st, nullptr);
+  if (rc) return rc;
+  moe_gemm_args d{};
+  d.op = MOE_OP_DOWN_WEIGHTED;
+  d.a = at<void>(ws, L.h);
+  d.offsets = at<int32_t>(ws, L.offsets);
+  d.w = w->w_down;
+  d.w_scales = w->s_down;
+  d.perm_pair = at<int32_t>(ws, L.perm);
+  d.blob = at<int32_t>(ws, L.blob);
+  d.out = at<void>(ws, L.o);
+  d.a_shared = at<void>(ws, L.hs);
+  d.w_shared = w->ws_down;
+  d.ws_scales = w->ss_down;
+  d.out_shared = at<void>(ws, L.os);
+  rc = gemm_impl(c, dev, &d, ws, L, st, nullptr);
+  if (rc) return rc;
+  launch_combine(at<float>(ws, L.o), at<float>(ws, L.os), at<int32_t>(ws, L.inv), c->T, c->D,
+                 c->k, y, st);
+  return cuda_rc(cudaGetLastError());
+}
+
+int begin(const moe_config* c, int entry, void* ws, size_t ws_bytes, DevInfo* dev, Layout* L) {
+  int rc = validate(c);
+  if (rc) return rc;
+  *L = layout(c, entry);
+  if (!ws || ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_ALIGN;
+  return current_device(dev);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config* cfg, int entry) {
+  if (validate(cfg) != MOE_OK) return 0;
+  if (entry < MOE_ENTRY_ROUTE || entry > MOE_ENTRY_FORWARD_HOST) return 0;
+  return layout(cfg, entry).total;
+}
+
+int moe_route(const moe_config* cfg, const void* x, const void* w_router, const float* bias,
+              int32_t* blob, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !w_router || !blob) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(blob) || (bias && !aligned16(bias)))
+    return MOE_ERR_ALIGN;
+  DevInfo dev;
+  Layout L;
+  int rc = begin(cfg, MOE_ENTRY_ROUTE, ws, ws_bytes, &dev, &L);
+  if (rc) return rc;
+  return route_impl(cfg, dev, x, w_router, bias, blob, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int32_t* offsets,
+                int32_t* perm_pair, int32_t* inv_row, void* ws, size_t ws_bytes, void* stream) {
+  if (!blob || !counts || !offsets || !perm_pair || !inv_row) return MOE_ERR_INVALID_ARG;
+  DevInfo dev;
+  Layout L;
+  int rc = begin(cfg, MOE_ENTRY_PERMUTE, ws, ws_bytes, &dev, &L);
+  if (rc) return rc;
+  return cuda_rc(launch_permute(blob, cfg->T, cfg->k, cfg->E, at<int32_t>(ws, L.chunk), counts,
+                                offsets, perm_pair, inv_row, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws, size_t ws_bytes,
+                     void* stream) {
+  int rc = validate(cfg);
+  if (rc) return rc;
+  rc = check_gemm_args(cfg, args);
+  if (rc) return rc;
+  DevInfo dev;
+  Layout L;
+  rc = begin(cfg, MOE_ENTRY_GROUPED_GEMM, ws, ws_bytes, &dev, &L);
+  if (rc) return rc;
+  if (cudaMemsetAsync(ws, 0, 8, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return gemm_impl(cfg, dev, args, ws, L, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int moe_combine(const moe_config* cfg, const float* o, const float* o_shared,
+                const int32_t* inv_row, void* y, void* stream) {
+  int rc = validate(cfg);
+  if (rc) return rc;
+  if (!o || !inv_row || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(y) || (o_shared && !aligned16(o_shared))) return MOE_ERR_ALIGN;
+  DevInfo dev;
+  rc = current_device(&dev);
+  if (rc) return rc;
+  launch_combine(o, o_shared, inv_row, cfg->T, cfg->D, cfg->k, y,
+                 static_cast<cudaStream_t>(stream));
+  return cuda_rc(cudaGetLastError());
+}
+
+int moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* y, void* ws,
+                size_t ws_bytes, void* stream) {
+  int rc = validate(cfg);
+  if (rc) return rc;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return MOE_ERR_ALIGN;
+  rc = check_weights(cfg, w);
+  if (rc) return rc;
+  DevInfo dev;
+  Layout L;
+  rc = begin(cfg, MOE_ENTRY_FORWARD, ws, ws_bytes, &dev, &L);
+  if (rc) return rc;
+  return forward_impl(cfg, dev, x, w, y, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w, void* y_host,
+                     void* ws, size_t ws_bytes, void* stream) {
+  int rc = validate(cfg);
+  if (rc) return rc;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  rc = check_weights(cfg, w);
+  if (rc) return rc;
+  DevInfo dev;
+  Layout L;
+  rc = begin(cfg, MOE_ENTRY_FORWARD_HOST, ws, ws_bytes, &dev, &L);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = static_cast<size_t>(cfg->T) * cfg->D * 2;
+  void* xd = at<void>(ws, L.xin);
+  void* yd = at<void>(ws, L.yout);
+  if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  rc = forward_impl(cfg, dev, xd, w, yd, ws, L, st);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_get_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int h = 0;
+  if (cudaMemcpyAsync(&h, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h != 0 && cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  return h;
+}
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "success";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape, format or device";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// kernels.h -- host-side launch functions of the libmoe_gb300 kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kPermuteChunk = 2048;  // pairs per permute block
+
+// ---- router (router.cu)
+void launch_row_norms(const void* a, int rows, int cols, float* out, cudaStream_t st);
+void launch_router_logits(const void* x, const void* wr, int T, int D, int E, int S,
+                          int sub_per_split, float* z_part, cudaStream_t st);
+cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
+                                 const float* bias, const float* xnorm, const float* wnorm,
+                                 float gamma, const void* x, const void* wr, int32_t* blob,
+                                 int* refine_count, cudaStream_t st);
+
+// ---- dispatch (permute.cu)
+cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,
+                           int32_t* counts, int32_t* offsets, int32_t* perm_pair,
+                           int32_t* inv_row, cudaStream_t st);
+void launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div, void* out,
+                        cudaStream_t st);
+
+// ---- combine (combine.cu)
+void launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T, int D,
+                    int k, void* y, cudaStream_t st);
+
+// ---- grouped GEMM (grouped_gemm.cu)
+enum GemmOp : int { kOpGateUp = 0, kOpDown = 1 };
+
+// Scalar parameters of one persistent grouped-GEMM launch.  Group order for
+// the tile walk: the shared group first (if any), then routed experts 0..E-1.
+struct GemmParams {
+  int op;
+  int E;
+  int has_shared;
+  int T_shared;             // rows of the shared group
+  const int32_t* offsets;   // [E+1] routed group row ranges
+  int m_tiles, m_tiles_s;   // weight-row tiles per group (gate/up: I/64, down: D/128)
+  int k_blocks, k_blocks_s; // K / 64
+  int a_rows_per_expert;    // rows of one expert in the routed weight map (2I or D)
+  int ld_out, ld_out_s;     // output row strides (elements)
+  void* out;                // gate/up: bf16 [rows][I]; down: fp32 [rows][D]
+  void* out_s;
+  const int32_t* perm_pair; // down: grouped row -> pair
+  const int32_t* blob;      // down: weights
+  int k;
+  int* status;              // workspace status word
+  // W4A16 only
+  const int32_t* wq;        // packed routed weights (row-major [rows][K/8])
+  const uint16_t* wscale;   // routed scales [rows][K/group]
+  const int32_t* wq_s;
+  const uint16_t* wscale_s;
+  int K, K_s;               // reduction sizes (elements)
+  int group;
+};
+
+struct GemmMaps {
+  CUtensorMap a, a_s, b, b_s;  // weights (routed, shared), activations (routed, shared)
+};
+
+// Kernel variants: BN_MAX token rows per tile (64 or 256); quant 0 = bf16, 1 = W4A16.
+cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int bn_max, int quant,
+                                int num_sms, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,172 @@
+// permute.cu -- dispatch: group (token, slot) pairs by expert; gather rows.
+//
+// "Systems engineering playbook: optimizing Qwen 3.5-397B MoE on Ironwood
+// (TPU7x)", section 3, "Option B": every device filters and computes the inputs
+// routed to its own experts.  On one GPU that is a stable grouping of the
+// T*k pairs p = t*k + j by expert id: an expert histogram, an exclusive scan
+// and a stable scatter.  All three steps are integer-exact and deterministic.
+//
+// Work split: pairs are cut into chunks of kChunk; chunk b counts its experts
+// (count kernel), one block turns the [chunks][E] table into per-chunk base
+// positions plus counts/offsets (scan kernel), and each chunk places its pairs
+// in order (scatter kernel: per-warp segments, __match_any_sync for ranks
+// within a step of 32).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__device__ __forceinline__ int pair_expert(const int32_t* __restrict__ blob, int k, int p) {
+  const int t = p / k, j = p - t * k;
+  return blob[static_cast<size_t>(t) * 2 * k + j];
+}
+
+__global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __restrict__ blob,
+                                                            int P, int k, int E,
+                                                            int32_t* __restrict__ chunk_cnt) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kPermuteChunk;
+  const int p1 = min(P, p0 + kPermuteChunk);
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) atomicAdd(&hist[pair_expert(blob, k, p)], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_cnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// One block of 1024 threads.  On exit chunk_cnt[b][e] holds the first grouped
+// row of chunk b's pairs for expert e.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ chunk_cnt,
+                                                            int B, int E,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int e0 = 0; e0 < E; e0 += 1024) {
+    const int e = e0 + threadIdx.x;
+    int total = 0;
+    if (e < E) {
+      for (int b = 0; b < B; ++b) {
+        const size_t i = static_cast<size_t>(b) * E + e;
+        const int c = chunk_cnt[i];
+        chunk_cnt[i] = total;
+        total += c;
+      }
+      counts[e] = total;
+    }
+    // block-wide exclusive scan of `total` over e
+    int incl = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int s = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += n;
+      }
+      warp_sums[lane] = s;  // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = carry + (wid ? warp_sums[wid - 1] : 0) + incl - total;
+    if (e < E) {
+      offsets[e] = excl;
+      for (int b = 0; b < B; ++b) chunk_cnt[static_cast<size_t>(b) * E + e] += excl;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry += warp_sums[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) offsets[E] = carry;
+}
+
+// 256 threads = 8 warps; warp w owns pairs [p0 + w*seg, p0 + (w+1)*seg) of the chunk.
+__global__ void __launch_bounds__(256) permute_scatter_kernel(
+    const int32_t* __restrict__ blob, int P, int k, int E, const int32_t* __restrict__ chunk_base,
+    int32_t* __restrict__ perm_pair, int32_t* __restrict__ inv_row) {
+  extern __shared__ int wcnt[];  // [8][E]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  constexpr int seg = kPermuteChunk / 8;
+  const int p0 = blockIdx.x * kPermuteChunk + wid * seg;
+  const int p1 = min(P, p0 + seg);
+  for (int p = p0 + lane; p < p1; p += 32) atomicAdd(&wcnt[wid * E + pair_expert(blob, k, p)], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = chunk_base[static_cast<size_t>(blockIdx.x) * E + e];
+    for (int w = 0; w < 8; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  int* my = wcnt + wid * E;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const bool valid = p < p1;
+    const int e = valid ? pair_expert(blob, k, p) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int pos = 0;
+    if (valid) pos = my[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0) my[e] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      perm_pair[pos] = p;
+      inv_row[p] = pos;
+    }
+  }
+}
+
+// out[r][:] = a[idx[r] / div][:]  (D bf16 per row, 16-byte vectors).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ a,
+                                                          const int32_t* __restrict__ idx,
+                                                          int rows, int vec_per_row, int div,
+                                                          uint4* __restrict__ out) {
+  const int r = blockIdx.x;
+  if (r >= rows) return;
+  const int src = idx[r] / div;
+  const uint4* s = a + static_cast<size_t>(src) * vec_per_row;
+  uint4* d = out + static_cast<size_t>(r) * vec_per_row;
+  for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = __ldg(s + i);
+}
+
+cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,
+                           int32_t* counts, int32_t* offsets, int32_t* perm_pair,
+                           int32_t* inv_row, cudaStream_t st) {
+  const int P = T * k;
+  const int B = (P + kPermuteChunk - 1) / kPermuteChunk;
+  const size_t smem_count = static_cast<size_t>(E) * sizeof(int);
+  const size_t smem_scatter = static_cast<size_t>(8) * E * sizeof(int);
+  if (smem_scatter > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(permute_scatter_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_scatter));
+    if (e != cudaSuccess) return e;
+  }
+  permute_count_kernel<<<B, 256, smem_count, st>>>(blob, P, k, E, chunk_cnt);
+  permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_cnt, B, E, counts, offsets);
+  permute_scatter_kernel<<<B, 256, smem_scatter, st>>>(blob, P, k, E, chunk_cnt, perm_pair,
+                                                       inv_row);
+  return cudaGetLastError();
+}
+
+void launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div, void* out,
+                        cudaStream_t st) {
+  gather_rows_kernel<<<rows, 256, 0, st>>>(static_cast<const uint4*>(a), idx, rows, D / 8, div,
+                                           static_cast<uint4*>(out));
+}
+
+}  // namespace moe

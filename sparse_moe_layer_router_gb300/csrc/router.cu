@@ -1,0 +1,375 @@
+// router.cu -- softmax router with top-k selection (sm_103a).
+//
+// "Systems engineering playbook: optimizing Qwen 3.5-397B MoE on Ironwood
+// (TPU7x)", section 1, "Sparse Mixture-of-Experts (MoE)": the router gate
+// projects the token representation, forms a softmax over the experts and
+// keeps the top-k routed experts; the selected probabilities are renormalised.
+// Section 3, "3-to-2 All-Gather optimisation": ids and weights are packed into
+// one int32 blob [T][2][k].
+//
+// Routing decision.  The deciding logit is defined as the fp64 sum, in index
+// order, of the exact products x[t,d]*Wr[e,d] (plus the fp32 bias, added
+// last).  The GPU computes fp32 logits v with a summation tree of bounded
+// depth h, so |v - z| <= r = gamma_h * ||x_t|| * ||Wr_e|| + 2^-23 |v| (the
+// Cauchy-Schwarz bound on sum |x_d Wr_ed|, plus the fp64 definition's own
+// deviation folded into gamma).  A token whose k-th / (k+1)-th boundary is
+// separated by these intervals is certified; otherwise the experts whose
+// intervals straddle the boundary are recomputed with the defining fp64
+// index-order sum and the boundary is re-decided exactly (ties: lower index).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- norms
+// out[row] >= || a[row, :] ||_2 (rigorous upper bound; see the margin below).
+__global__ void __launch_bounds__(256) row_norm_bound_kernel(const __nv_bfloat16* __restrict__ a,
+                                                             int rows, int cols,
+                                                             float* __restrict__ out) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint4* p = reinterpret_cast<const uint4*>(a + static_cast<size_t>(row) * cols);
+  float s = 0.f;
+  for (int i = lane; i < cols / 8; i += 32) {
+    const uint4 v = __ldg(p + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16);
+      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      s = fmaf(lo, lo, s);
+      s = fmaf(hi, hi, s);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) {
+    // Sum of non-negative terms with chain length <= cols/32*... + 5: relative
+    // error below 2^-10 for cols <= 2^16; sqrt and products add 2^-20 slack.
+    out[row] = sqrtf(s * (1.0f + 0x1p-10f)) * (1.0f + 0x1p-20f);
+  }
+}
+
+// ---------------------------------------------------------------- logits
+// z_part[split][t][e] = sum over the split's K range of x[t,k] * Wr[e,k] (fp32).
+// Within the range, products are accumulated in sub-chunks of 64 (a fresh fp32
+// accumulator each), and sub-chunk sums are added to the running total: each
+// product passes through at most 64 + sub_per_split roundings.
+constexpr int kRT = 64, kRE = 64, kRK = 32;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wr, int T, int D,
+    int E, int sub_per_split, float* __restrict__ z_part) {
+  __shared__ __align__(16) float xs[kRK][kRT + 4];
+  __shared__ __align__(16) float ws[kRK][kRE + 4];
+  const int e0 = blockIdx.x * kRE, t0 = blockIdx.y * kRT, split = blockIdx.z;
+  const int nsub = D / 64;
+  const int sub_begin = split * sub_per_split;
+  const int sub_end = min(nsub, sub_begin + sub_per_split);
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int lrow = tid >> 2, lk = (tid & 3) * 8;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+  for (int sub = sub_begin; sub < sub_end; ++sub) {
+    float part[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      const int kbase = sub * 64 + half * 32;
+      uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
+      if (t0 + lrow < T)
+        xv = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + lrow) * D + kbase +
+                                                  lk));
+      if (e0 + lrow < E)
+        wv = __ldg(reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e0 + lrow) * D +
+                                                  kbase + lk));
+      __syncthreads();
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xs[lk + 2 * j][lrow] = __uint_as_float(xw[j] << 16);
+        xs[lk + 2 * j + 1][lrow] = __uint_as_float(xw[j] & 0xFFFF0000u);
+        ws[lk + 2 * j][lrow] = __uint_as_float(ww[j] << 16);
+        ws[lk + 2 * j + 1][lrow] = __uint_as_float(ww[j] & 0xFFFF0000u);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < kRK; ++kk) {
+        const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+        const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] += part[i][j];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+    float* dst = z_part + (static_cast<size_t>(split) * T + t) * E;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) dst[e] = acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- select
+// The defining logit: fp64 sum in index order of exact bf16 products (+ bias).
+__device__ double exact_logit(const __nv_bfloat16* __restrict__ xr,
+                              const __nv_bfloat16* __restrict__ wrow, int D,
+                              const float* __restrict__ bias, int e) {
+  double acc = 0.0;
+  const uint4* xp = reinterpret_cast<const uint4*>(xr);
+  const uint4* wp = reinterpret_cast<const uint4*>(wrow);
+  for (int i = 0; i < D / 8; ++i) {
+    const uint4 xv = __ldg(xp + i), wv = __ldg(wp + i);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // element 2j is the low half, 2j+1 the high half (little endian)
+      acc = fma(static_cast<double>(__uint_as_float(xw[j] << 16)),
+                static_cast<double>(__uint_as_float(ww[j] << 16)), acc);
+      acc = fma(static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u)),
+                static_cast<double>(__uint_as_float(ww[j] & 0xFFFF0000u)), acc);
+    }
+  }
+  if (bias) acc += static_cast<double>(bias[e]);
+  return acc;
+}
+
+// Order used for selection: larger value first, lower index on an exact tie.
+__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
+  return v > bv || (v == bv && e < be);
+}
+__device__ __forceinline__ bool better_d(double v, int e, double bv, int be) {
+  return v > bv || (v == bv && e < be);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) router_select_kernel(
+    const float* __restrict__ z_part, int S, int T, int D, int E, int k,
+    const float* __restrict__ bias, const float* __restrict__ xnorm,
+    const float* __restrict__ wnorm, float gamma, const __nv_bfloat16* __restrict__ x,
+    const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
+    int* __restrict__ refine_count) {
+  extern __shared__ double zx_smem[];  // [8 warps][E] refined logits
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + wib;
+  if (t >= T) return;
+  double* zx = zx_smem + static_cast<size_t>(wib) * E;
+
+  float v[VPL], r[VPL];
+  uint32_t sel = 0, cand = 0;
+  const float xn = xnorm[t];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      float s = 0.f;
+      for (int sp = 0; sp < S; ++sp) s += z_part[(static_cast<size_t>(sp) * T + t) * E + e];
+      if (bias) s += bias[e];
+      v[i] = s;
+      r[i] = gamma * xn * wnorm[e] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(s);
+    } else {
+      v[i] = -INFINITY;
+      r[i] = 0.f;
+    }
+  }
+
+  // k rounds of warp arg-max under (value desc, index asc).
+  float min_lo = INFINITY;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((sel >> i) & 1u) && better(v[i], e, bv, be)) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) {
+      const int i = be >> 5;
+#pragma unroll
+      for (int q = 0; q < VPL; ++q)
+        if (q == i) {
+          sel |= 1u << q;
+          min_lo = fminf(min_lo, v[q] - r[q]);
+        }
+    }
+  }
+  float max_hi = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && !((sel >> i) & 1u)) max_hi = fmaxf(max_hi, v[i] + r[i]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    min_lo = fminf(min_lo, __shfl_xor_sync(0xffffffffu, min_lo, o));
+    max_hi = fmaxf(max_hi, __shfl_xor_sync(0xffffffffu, max_hi, o));
+  }
+
+  if (!(min_lo > max_hi)) {
+    // Not certified: experts whose interval reaches across the boundary.
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= E) continue;
+      const bool s_in = (sel >> i) & 1u;
+      if ((s_in && v[i] - r[i] <= max_hi) || (!s_in && v[i] + r[i] >= min_lo)) cand |= 1u << i;
+    }
+    int slots = __popc(sel & cand);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) slots += __shfl_xor_sync(0xffffffffu, slots, o);
+    if (lane == 0 && refine_count) atomicAdd(refine_count, 1);
+    const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if ((cand >> i) & 1u) zx[e] = exact_logit(xr, wr + static_cast<size_t>(e) * D, D, bias, e);
+    }
+    __syncwarp();
+    sel &= ~cand;  // candidates compete for the remaining slots on exact values
+    uint32_t chosen = 0;
+    for (int j = 0; j < slots; ++j) {
+      double bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (((cand >> i) & 1u) && !((chosen >> i) & 1u) && better_d(zx[e], e, bv, be)) {
+          bv = zx[e];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (better_d(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+    }
+    sel |= chosen;
+    // Refined logits replace the fp32 ones for the weights.
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if ((cand >> i) & 1u) v[i] = static_cast<float>(zx[e]);
+    }
+  }
+
+  // Softmax over all E, renormalised over the selected k:
+  //   w_j = exp(v_j - m) / sum_selected exp(v_i - m)   (the full denominator cancels).
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float ex[VPL];
+  float den = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    ex[i] = ((sel >> i) & 1u) ? expf(v[i] - m) : 0.f;
+    den += ex[i];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+
+  // Ascending expert order: e = lane + 32 i, so scan i outer, lanes inner.
+  int32_t* out = blob + static_cast<size_t>(t) * 2 * k;
+  int base = 0;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const bool s_in = (sel >> i) & 1u;
+    const uint32_t bal = __ballot_sync(0xffffffffu, s_in);
+    if (s_in) {
+      const int pos = base + __popc(bal & lt_mask);
+      out[pos] = lane + 32 * i;
+      out[k + pos] = __float_as_int(ex[i] / den);
+    }
+    base += __popc(bal);
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+void launch_row_norms(const void* a, int rows, int cols, float* out, cudaStream_t st) {
+  const int warps_per_block = 8;
+  const int blocks = (rows + warps_per_block - 1) / warps_per_block;
+  row_norm_bound_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a), rows, cols,
+                                                out);
+}
+
+void launch_router_logits(const void* x, const void* wr, int T, int D, int E, int S,
+                          int sub_per_split, float* z_part, cudaStream_t st) {
+  dim3 grid((E + kRE - 1) / kRE, (T + kRT - 1) / kRT, S);
+  router_logits_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                             static_cast<const __nv_bfloat16*>(wr), T, D, E,
+                                             sub_per_split, z_part);
+}
+
+cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
+                                 const float* bias, const float* xnorm, const float* wnorm,
+                                 float gamma, const void* x, const void* wr, int32_t* blob,
+                                 int* refine_count, cudaStream_t st) {
+  const int blocks = (T + 7) / 8;
+  const size_t smem = static_cast<size_t>(8) * E * sizeof(double);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  const auto* wb = static_cast<const __nv_bfloat16*>(wr);
+#define MOE_SELECT_CASE(V)                                                                   \
+  if (E <= 32 * (V)) {                                                                       \
+    if (smem > 48 * 1024) {                                                                  \
+      cudaError_t e_ = cudaFuncSetAttribute(router_select_kernel<V>,                         \
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                                            static_cast<int>(smem));                         \
+      if (e_ != cudaSuccess) return e_;                                                      \
+    }                                                                                        \
+    router_select_kernel<V><<<blocks, 256, smem, st>>>(z_part, S, T, D, E, k, bias, xnorm,   \
+                                                       wnorm, gamma, xb, wb, blob,           \
+                                                       refine_count);                        \
+    return cudaGetLastError();                                                               \
+  }
+  MOE_SELECT_CASE(1)
+  MOE_SELECT_CASE(4)
+  MOE_SELECT_CASE(16)
+  MOE_SELECT_CASE(32)
+#undef MOE_SELECT_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

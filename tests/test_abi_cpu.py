@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/moe.h declares, sizes workspaces, and rejects invalid
+arguments on the host (before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_layer_router_gb300 import binding as B
+from sparse_moe_layer_router_gb300.build import build
+from sparse_moe_layer_router_gb300.synthetic import CONFIGS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return B.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert set(names) == set(B.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_sizes(lib):
+    for name, cfg in CONFIGS.items():
+        for entry in range(5):
+            n = B.workspace_size(cfg, entry)
+            assert n >= 256 and n % 256 == 0, (name, entry, n)
+        fwd = B.workspace_size(cfg, B.MOE_ENTRY_FORWARD)
+        host = B.workspace_size(cfg, B.MOE_ENTRY_FORWARD_HOST)
+        assert host >= fwd + 2 * 2 * cfg.T * cfg.D
+    assert B.workspace_size(CONFIGS["tiny"], 99) == 0
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("k", 0, B.MOE_ERR_INVALID_ARG),
+    ("k", 17, B.MOE_ERR_INVALID_ARG),     # k > E
+    ("T", 0, B.MOE_ERR_INVALID_ARG),
+    ("D", 200, B.MOE_ERR_UNSUPPORTED),    # not a multiple of 128
+    ("I", 100, B.MOE_ERR_UNSUPPORTED),    # not a multiple of 64
+    ("E", 2000, B.MOE_ERR_UNSUPPORTED),
+    ("quant", 7, B.MOE_ERR_UNSUPPORTED),
+])
+def test_invalid_config_rejected_on_host(lib, field, value, code):
+    cfg = B.config(CONFIGS["tiny"])
+    setattr(cfg, field, value)
+    assert lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_FORWARD) == 0
+    dummy = ctypes.c_void_p(4096)
+    rc = lib.moe_route(ctypes.byref(cfg), dummy, dummy, None, dummy, dummy, 1 << 30, None)
+    assert rc == code
+
+
+def test_w4a16_group_must_be_128(lib):
+    cfg = B.config(CONFIGS["w4a16"])
+    cfg.group = 64
+    assert lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_FORWARD) == 0
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    cfg = B.config(CONFIGS["tiny"])
+    d = ctypes.c_void_p(4096)
+    assert lib.moe_route(ctypes.byref(cfg), None, d, None, d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    odd = ctypes.c_void_p(4096 + 2)
+    assert lib.moe_route(ctypes.byref(cfg), odd, d, None, d, d, 1 << 30, None) == B.MOE_ERR_ALIGN
+    assert lib.moe_permute(ctypes.byref(cfg), None, d, d, d, d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    w = B.MoeWeights()
+    assert lib.moe_forward(ctypes.byref(cfg), d, ctypes.byref(w), d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    args = B.MoeGemmArgs()
+    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_small_workspace_rejected(lib):
+    cfg = B.config(CONFIGS["tiny"])
+    d = ctypes.c_void_p(4096)
+    need = lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_ROUTE)
+    assert lib.moe_route(ctypes.byref(cfg), d, d, None, d, d, need - 1, None) == B.MOE_ERR_WORKSPACE
+
+
+def test_bf16_weights_with_scales_rejected(lib):
+    cfg = B.config(CONFIGS["tiny"])
+    d = ctypes.c_void_p(4096)
+    w = B.MoeWeights(d, None, d, d, d, None, d, d, None, None)
+    assert lib.moe_forward(ctypes.byref(cfg), d, ctypes.byref(w), d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_strerror(lib):
+    for c in (0, -1, -2, -3, -4, -5, -6):
+        assert B.strerror(c) and B.strerror(c) != "unknown error"
+    assert B.strerror(-99) == "unknown error"

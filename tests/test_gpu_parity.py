@@ -1,0 +1,229 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Routing ids, counts, offsets and permutations must match bit for bit; blob
+weights within 1e-5; layer outputs within max|err| <= 2e-2 max|ref| and
+sum|err| / sum|ref| <= 5e-3.  Inputs come from the seeded generator; expected
+values come only from the oracle, computed on host copies of the same inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_moe_layer_router_gb300 import binding as B
+from sparse_moe_layer_router_gb300.build import build
+from sparse_moe_layer_router_gb300.synthetic import (CONFIGS, MoEConfig, as_u16, make_inputs,
+                                                     normal_bf16)
+
+from helpers import (WEIGHT_ABS, blob_parts, expert_host, oracle_layer_rows, oracle_route,
+                     tol_check, y_host)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny": CONFIGS["tiny"],
+    # several tiles in every direction with a ragged tail
+    "ragged": MoEConfig("ragged", T=37, D=256, E=24, I=192, Is=128, k=3),
+    # k = E: every token uses every expert
+    "all_experts": MoEConfig("all_experts", T=50, D=128, E=4, I=64, Is=64, k=4),
+    "one_token": MoEConfig("one_token", T=1, D=384, E=32, I=128, Is=64, k=5),
+    # hot experts (> 64 rows: several token tiles) and a 200-row shared group
+    "hot": MoEConfig("hot", T=200, D=256, E=16, I=128, Is=128, k=2, zipf_s=1.2, zipf_alpha=3.0),
+    # the 256-row token tile variant
+    "wide": MoEConfig("wide", T=2100, D=256, E=8, I=64, Is=64, k=2),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built(cuda_ok):
+    build()
+    B.lib()
+
+
+def gpu_inputs(cfg):
+    host = make_inputs(cfg, device="cpu")
+    return host, host.to("cuda")
+
+
+def check_route(cfg, host, dev, expect_refine=None):
+    ws = B.workspace(cfg, B.MOE_ENTRY_ROUTE)
+    blob = B.route(cfg, dev.x, dev.w_router, dev.bias, ws=ws)
+    torch.cuda.synchronize()
+    ids, w = blob_parts(blob)
+    ids_ref, w_ref = oracle_route(host)
+    mism = np.argwhere(ids != ids_ref)
+    assert mism.size == 0, f"{len(mism)} id mismatches, first at {mism[:3].tolist()}"
+    np.testing.assert_allclose(w, w_ref, rtol=0, atol=WEIGHT_ABS)
+    refined = int(ws[4:8].view(torch.int32).item())
+    if expect_refine is not None:
+        assert (refined > 0) == expect_refine, refined
+    return blob, ids_ref, w_ref, refined
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_route_bit_exact(name):
+    cfg = SMALL[name]
+    host, dev = gpu_inputs(cfg)
+    check_route(cfg, host, dev)
+
+
+def test_route_zero_router_ties_go_to_lower_index():
+    cfg = SMALL["ragged"]
+    host, dev = gpu_inputs(cfg)
+    host.w_router.zero_()
+    dev.w_router.zero_()
+    blob, ids_ref, w_ref, _ = check_route(cfg, host, dev)
+    assert (ids_ref == np.arange(cfg.k)).all()
+
+
+def test_route_near_ties_refined_exactly():
+    """Router rows that differ in one element by one bf16 step: fp32 cannot
+    certify the boundary, so the fp64 re-decision must reproduce the oracle."""
+    cfg = MoEConfig("near_tie", T=64, D=512, E=64, I=64, Is=64, k=6)
+    host, dev = gpu_inputs(cfg)
+    base = host.w_router[0].clone()
+    wr = base.repeat(cfg.E, 1)
+    for e in range(cfg.E):
+        d = (7 * e) % cfg.D
+        wr[e, d] = torch.nextafter(base[d].float(), torch.tensor(float("inf"))).to(torch.bfloat16) \
+            if e % 2 else base[d]
+    wr[5] = wr[3]  # an exact duplicate: exact tie decided by index
+    host.w_router.copy_(wr)
+    dev.w_router.copy_(wr.cuda())
+    _, _, _, refined = check_route(cfg, host, dev, expect_refine=True)
+    assert refined > 0
+
+
+def test_route_with_bias():
+    cfg = SMALL["hot"]
+    host, dev = gpu_inputs(cfg)
+    assert host.bias is not None
+    check_route(cfg, host, dev)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "hot", "wide"])
+def test_permute_bit_exact(name):
+    cfg = SMALL[name]
+    host, _ = gpu_inputs(cfg)
+    ids, w = oracle_route(host)
+    blob = torch.from_numpy(oracle.pack_blob(ids, w)).cuda()
+    counts, offsets, perm, inv = B.permute(cfg, blob)
+    c_ref, o_ref, p_ref, i_ref = oracle.permute(ids, cfg.E)
+    assert (counts.cpu().numpy() == c_ref).all()
+    assert (offsets.cpu().numpy() == o_ref).all()
+    assert (perm.cpu().numpy() == p_ref).all()
+    assert (inv.cpu().numpy() == i_ref).all()
+
+
+def test_permute_random_ids_properties_large():
+    """Random distinct ids per token at a size spanning many permute chunks."""
+    T, E, k = 5000, 300, 7
+    rng = np.random.default_rng(11)
+    ids = np.sort(np.argsort(rng.random((T, E)), axis=1)[:, :k], axis=1).astype(np.int32)
+    cfg = MoEConfig("perm", T=T, D=128, E=E, I=64, Is=64, k=k)
+    blob = torch.from_numpy(oracle.pack_blob(ids, np.full((T, k), 1.0 / k))).cuda()
+    counts, offsets, perm, inv = B.permute(cfg, blob)
+    c_ref, o_ref, p_ref, i_ref = oracle.permute(ids, E)
+    assert (counts.cpu().numpy() == c_ref).all()
+    assert (offsets.cpu().numpy() == o_ref).all()
+    assert (perm.cpu().numpy() == p_ref).all()
+    assert (inv.cpu().numpy() == i_ref).all()
+
+
+def grouped_setup(cfg):
+    host, dev = gpu_inputs(cfg)
+    ids, w = oracle_route(host)
+    counts, offsets, perm, inv = oracle.permute(ids, cfg.E)
+    blob = oracle.pack_blob(ids, w)
+    return host, dev, ids, w, offsets, perm, inv, blob
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "hot", "wide", "one_token"])
+def test_grouped_gate_up_swiglu(name):
+    cfg = SMALL[name]
+    host, dev, ids, w, offsets, perm, inv, blob = grouped_setup(cfg)
+    P = cfg.T * cfg.k
+    tok = perm // cfg.k
+    h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device="cuda")
+    hs = torch.empty((cfg.T, cfg.Is), dtype=torch.bfloat16, device="cuda")
+    B.grouped_gemm(cfg, B.MOE_OP_GATE_UP_SWIGLU, dev.x, torch.from_numpy(offsets).cuda(),
+                   dev.w_gate_up, h, a_row_index=torch.from_numpy(tok.astype(np.int32)).cuda(),
+                   a_shared=dev.x, w_shared=dev.ws_gate_up, out_shared=hs)
+    torch.cuda.synchronize()
+    xh = as_u16(host.x)
+    ref = np.empty((P, cfg.I))
+    for e in range(cfg.E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            ref[r0:r1] = oracle.expert_hidden(xh[tok[r0:r1]], as_u16(host.w_gate_up[e]))
+    tol_check(y_host(h), ref, what="h")
+    ref_s = oracle.expert_hidden(xh, as_u16(host.ws_gate_up))
+    tol_check(y_host(hs), ref_s, what="h_shared")
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "hot", "wide"])
+def test_grouped_down_weighted(name):
+    cfg = SMALL[name]
+    host, dev, ids, w, offsets, perm, inv, blob = grouped_setup(cfg)
+    P = cfg.T * cfg.k
+    h = normal_bf16((P, cfg.I), 0.5, 3, 77)
+    hs = normal_bf16((cfg.T, cfg.Is), 0.5, 3, 78)
+    o = torch.empty((P, cfg.D), dtype=torch.float32, device="cuda")
+    os_ = torch.empty((cfg.T, cfg.D), dtype=torch.float32, device="cuda")
+    B.grouped_gemm(cfg, B.MOE_OP_DOWN_WEIGHTED, h.cuda(), torch.from_numpy(offsets).cuda(),
+                   dev.w_down, o, perm_pair=torch.from_numpy(perm).cuda(),
+                   blob=torch.from_numpy(blob).cuda(), a_shared=hs.cuda(), w_shared=dev.ws_down,
+                   out_shared=os_)
+    torch.cuda.synchronize()
+    hf = h.float().numpy().astype(np.float64)
+    wrow = blob[:, 1, :].view(np.float32).reshape(-1)[perm].astype(np.float64)
+    ref = np.empty((P, cfg.D))
+    for e in range(cfg.E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            ref[r0:r1] = oracle.expert_down(hf[r0:r1], as_u16(host.w_down[e])) * wrow[r0:r1, None]
+    tol_check(o.cpu().numpy(), ref, max_rel=1e-4, mean_rel=1e-5, what="o")
+    ref_s = oracle.expert_down(hs.float().numpy().astype(np.float64), as_u16(host.ws_down))
+    tol_check(os_.cpu().numpy(), ref_s, max_rel=1e-4, mean_rel=1e-5, what="o_shared")
+
+
+def test_combine():
+    cfg = SMALL["ragged"]
+    host, dev, ids, w, offsets, perm, inv, blob = grouped_setup(cfg)
+    P = cfg.T * cfg.k
+    g = torch.Generator().manual_seed(5)
+    o = torch.randn((P, cfg.D), generator=g)
+    osh = torch.randn((cfg.T, cfg.D), generator=g)
+    y = B.combine(cfg, o.cuda(), osh.cuda(), torch.from_numpy(inv).cuda())
+    ref = oracle.combine(o.numpy().astype(np.float64), osh.numpy().astype(np.float64), inv, cfg.k)
+    tol_check(y_host(y), ref, max_rel=4e-3, mean_rel=2e-3, what="y")
+    y0 = B.combine(cfg, o.cuda(), None, torch.from_numpy(inv).cuda())
+    ref0 = oracle.combine(o.numpy().astype(np.float64), None, inv, cfg.k)
+    tol_check(y_host(y0), ref0, max_rel=4e-3, mean_rel=2e-3, what="y (no shared)")
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_parity(name):
+    cfg = SMALL[name]
+    host, dev = gpu_inputs(cfg)
+    ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
+    y = B.forward(cfg, dev.x, dev, ws=ws)
+    assert B.get_status(ws) == B.MOE_OK
+    ids, w = oracle_route(host)
+    ref = oracle_layer_rows(host, np.arange(cfg.T), ids, w)
+    tol_check(y_host(y), ref)
+
+
+def test_forward_deterministic_and_host_entry():
+    cfg = SMALL["hot"]
+    host, dev = gpu_inputs(cfg)
+    ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
+    y1 = B.forward(cfg, dev.x, dev, ws=ws).clone()
+    y2 = B.forward(cfg, dev.x, dev, ws=ws).clone()
+    assert torch.equal(y1, y2)
+    wsh = B.workspace(cfg, B.MOE_ENTRY_FORWARD_HOST)
+    xh = host.x.clone().pin_memory()
+    yh = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16).pin_memory()
+    B.forward_host(cfg, xh, dev, yh, wsh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y1.cpu())

@@ -409,3 +409,42 @@ def test_config_presets_match_pages_shapes():
                                          g["top_k"])
     assert CONFIGS["prefill"].T == g["tokens_per_core_batch"]
     assert CONFIGS["w4a16"].group == 128
+
+
+def test_expert_hidden_and_down_match_numpy():
+    """The per-expert halves: numpy matmuls + scipy logistic (bf16 and int4 weights)."""
+    D, I, n = 32, 16, 5
+    x = as_u16(normal_bf16((n, D), 1.0, 5, 51))
+    gu = as_u16(normal_bf16((2 * I, D), D ** -0.5, 5, 52))
+    dn = as_u16(normal_bf16((D, I), I ** -0.5, 5, 53))
+    h = oracle.expert_hidden(x, gu)
+    xf, G, Dn = u16_to_f64(x), u16_to_f64(gu), u16_to_f64(dn)
+    g, u = xf @ G[:I].T, xf @ G[I:].T
+    np.testing.assert_allclose(h, g * scipy.special.expit(g) * u, rtol=1e-12, atol=1e-14)
+    o = oracle.expert_down(h, dn)
+    np.testing.assert_allclose(o, h @ Dn.T, rtol=1e-12, atol=1e-14)
+    # int4 weights: the same against the hand-dequantised matrices
+    rng = np.random.default_rng(3)
+    qg = rng.integers(-8, 8, size=(2 * I, D))
+    sg = bf16_bits(rng.choice([0.5, 0.25, 0.125], size=(2 * I, D // 16)))
+    qd = rng.integers(-8, 8, size=(D, I))
+    sd = bf16_bits(rng.choice([0.5, 0.25, 0.125], size=(D, I // 16)))
+    Gq = qg * np.repeat(u16_to_f64(sg), 16, axis=1)
+    Dq = qd * np.repeat(u16_to_f64(sd), 16, axis=1)
+    h4 = oracle.expert_hidden(x, pack_by_hand(qg), sg, group=16)
+    g, u = xf @ Gq[:I].T, xf @ Gq[I:].T
+    np.testing.assert_allclose(h4, g * scipy.special.expit(g) * u, rtol=1e-12, atol=1e-14)
+    o4 = oracle.expert_down(h4, pack_by_hand(qd), sd, group=16)
+    np.testing.assert_allclose(o4, h4 @ Dq.T, rtol=1e-12, atol=1e-14)
+
+
+def test_combine_matches_fancy_index_sum():
+    rng = np.random.default_rng(7)
+    T, D, k = 11, 8, 3
+    o = rng.standard_normal((T * k, D))
+    osh = rng.standard_normal((T, D))
+    inv = rng.permutation(T * k).astype(np.int32)
+    y = oracle.combine(o, osh, inv, k)
+    np.testing.assert_allclose(y, osh + o[inv.reshape(T, k)].sum(axis=1), rtol=1e-14, atol=1e-14)
+    y0 = oracle.combine(o, None, inv, k)
+    np.testing.assert_allclose(y0, o[inv.reshape(T, k)].sum(axis=1), rtol=1e-14, atol=1e-14)
