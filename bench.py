@@ -1,0 +1,473 @@
+"""Benchmark of the MoE layer forward (decode step: T=64, D=4096, E=512, I=1024, top-10).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path
+(router -> dispatch -> grouped gate/up -> grouped down -> combine, shared
+expert included) over one batch of synthetic input, through the C ABI.
+
+  value     tokens/s of moe_forward with every input resident in HBM (K steps
+            timed with CUDA events between a barrier + synchronize on both sides;
+            the touched expert weights, ~9.3 GB per step, exceed L2, so no flush).
+  e2e       the same metric through moe_forward_host: pinned host x copied in and
+            y copied out inside every timed step.
+  roofline  the dominant kernel (grouped gate/up GEMM): algorithmic bytes per
+            launch / its mean CUDA-event duration inside a timed pass of the
+            path split into its ABI calls, against the measured HBM copy peak.
+  cpu_baseline  the fp64 oracle on this host's cores over the same batch.
+
+With --gpus N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica of the layer on its own GPU (the path has no exchange step
+on one device); value = all ranks' tokens / the slowest rank's time.
+``--impl reference`` times the fp64 oracle (the CPU reference) on the same
+workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (T=64 decode, T=1024 prefill) and % of HBM/BF16 roofline"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "grouped_gemm_gate_up_decode.md")
+GEMM_SOURCES = [os.path.join(ROOT, "sparse_moe_layer_router_gb300", "csrc", f)
+                for f in ("grouped_gemm.cu", "common.cuh")]
+L2_BYTES = 129 * 2**20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(cfg):
+    d = (f"{cfg.name}: T={cfg.T}, D={cfg.D}, E={cfg.E}, I={cfg.I}, Is={cfg.Is}, top-{cfg.k}, "
+         f"{'W4A16 int4 g128' if cfg.quant else 'bf16'} weights")
+    if cfg.zipf_s:
+        d += f", log-Zipf(s={cfg.zipf_s}) router bias x{cfg.zipf_alpha}"
+    return d
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, enabled=True):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        if not enabled:
+            return
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8], f[4]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ helpers
+def touched_gate_up_bytes(cfg, counts):
+    """Algorithmic HBM bytes of one grouped gate/up launch (see DESIGN)."""
+    import torch
+    touched = int((counts > 0).sum().item())
+    P = cfg.T * cfg.k
+    if cfg.quant == 0:
+        w_exp = 2 * cfg.I * cfg.D * 2
+        w_sh = 2 * cfg.Is * cfg.D * 2
+    else:
+        w_exp = 2 * cfg.I * cfg.D // 2 + 2 * cfg.I * (cfg.D // cfg.group) * 2
+        w_sh = 2 * cfg.Is * cfg.D // 2 + 2 * cfg.Is * (cfg.D // cfg.group) * 2
+    act = P * cfg.D * 2 + cfg.T * cfg.D * 2 + P * cfg.I * 2 + cfg.T * cfg.Is * 2
+    del torch
+    return touched * w_exp + w_sh + act, touched
+
+
+def layer_bytes_flops(cfg, touched):
+    """Algorithmic bytes / flops of one layer forward (touched weights + router + x + y)."""
+    if cfg.quant == 0:
+        per_exp = 3 * cfg.I * cfg.D * 2
+        sh = 3 * cfg.Is * cfg.D * 2
+    else:
+        per_exp = 3 * cfg.I * cfg.D // 2 + 3 * cfg.I * (cfg.D // cfg.group) * 2
+        sh = 3 * cfg.Is * cfg.D // 2 + 3 * cfg.Is * (cfg.D // cfg.group) * 2
+    byts = touched * per_exp + sh + cfg.E * cfg.D * 2 + 2 * cfg.T * cfg.D * 2
+    flops = (2 * cfg.T * cfg.D * cfg.E + 6 * cfg.T * cfg.k * cfg.D * cfg.I
+             + 6 * cfg.T * cfg.D * cfg.Is)
+    return byts, flops
+
+
+def profile_traffic():
+    """(traffic bytes per launch, ncu workload scale note) from the committed ncu summary,
+    or (None, why) when the kernel sources changed since the counters were taken."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None, "no committed ncu summary"
+    txt = open(PROFILE_SUMMARY).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    if not (m_sha and m_tr):
+        return None, "summary lacks traffic"
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        h.update(open(f, "rb").read())
+    if h.hexdigest() != m_sha.group(1):
+        return None, "kernel changed since the ncu capture"
+    return int(m_tr.group(1)), "ncu"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_pass(cfg, rows, host_x, host_wr, host_bias, experts, shared):
+    """The oracle's layer over the token rows ``rows``: routing, then the forward."""
+    import oracle
+    x = host_x[rows]
+    ids, w = oracle.route(x, host_wr, cfg.k, host_bias)
+    return oracle.forward(x, ids, w, experts, shared, E=cfg.E, I=cfg.I, Is=cfg.Is,
+                          quant=cfg.quant, group=cfg.group)
+
+
+def oracle_host_inputs(inp):
+    """Host copies of the inputs and of every expert the batch touches."""
+    import numpy as np
+    import oracle
+    from sparse_moe_layer_router_gb300.synthetic import as_u16
+    cfg = inp.cfg
+    x = as_u16(inp.x)
+    wr = as_u16(inp.w_router)
+    bias = None if inp.bias is None else inp.bias.cpu().numpy()
+    ids, _ = oracle.route(x, wr, cfg.k, bias)
+
+    def one(e):
+        if e == cfg.E:
+            t = (inp.ws_gate_up, inp.ws_down, inp.ss_gate_up, inp.ss_down)
+        else:
+            t = (inp.w_gate_up[e], inp.w_down[e],
+                 None if inp.s_gate_up is None else inp.s_gate_up[e],
+                 None if inp.s_down is None else inp.s_down[e])
+        if cfg.quant == 0:
+            return as_u16(t[0]), as_u16(t[1])
+        return t[0].cpu().numpy(), as_u16(t[2]), t[1].cpu().numpy(), as_u16(t[3])
+
+    experts = {int(e): one(int(e)) for e in np.unique(ids)}
+    return x, wr, bias, experts, one(cfg.E)
+
+
+def cpu_baseline(cfg, inputs, min_seconds=10.0, max_passes=20):
+    """Full-batch oracle passes until ``min_seconds`` of CPU work: (tokens/s, cores, passes)."""
+    import numpy as np
+    import oracle
+    rows = np.arange(cfg.T)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(cfg, rows, *inputs)
+        done += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or done >= max_passes:
+            return cfg.T * done / dt, oracle.num_threads(), done
+
+
+def run_reference(args, cfg, base_config, local):
+    """The reference arm: the fp64 oracle on the host cores, K timed steps of a
+    bounded token sample each (rotating through the batch)."""
+    import numpy as np
+    import torch
+    import oracle
+    from sparse_moe_layer_router_gb300.synthetic import make_inputs
+    oracle.build()
+    wdev = f"cuda:{local}" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(cfg, device="cpu", weight_device=wdev)
+    inputs = oracle_host_inputs(inp)
+    del inp
+    if torch.cuda.is_available():
+        torch.cuda.empty_cache()
+    cores = oracle.num_threads()
+    # size the per-step sample so that K + W steps take about two minutes
+    n0 = min(cfg.T, cores)
+    t1 = time.perf_counter()
+    oracle_pass(cfg, np.arange(n0), *inputs)
+    per_tok = (time.perf_counter() - t1) / n0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(cfg.T, budget / max(per_tok, 1e-9))))
+    W = max(3, args.warmup)
+
+    def rows(i):
+        return (np.arange(n) + i * n) % cfg.T
+
+    for i in range(W):
+        oracle_pass(cfg, rows(i), *inputs)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_pass(cfg, rows(W + i), *inputs)
+    dt = time.perf_counter() - t0
+    val = n * args.steps / dt
+    return {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": W, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init weights of the stated shapes)",
+            "config": base_config, "impl": "reference",
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} of the batch's {cfg.T} tokens per step (routing + "
+                                       f"layer, fp64), rotating through the batch"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse()
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+
+    from sparse_moe_layer_router_gb300 import binding as B
+    from sparse_moe_layer_router_gb300.build import build
+    from sparse_moe_layer_router_gb300.synthetic import CONFIGS, make_inputs
+
+    cfg = CONFIGS[args.config]
+    hbm_peak, bf16_peak, peak_src = peaks()
+    base_config = {"workload": workload_desc(cfg), "T": cfg.T, "D": cfg.D, "E": cfg.E,
+                   "I": cfg.I, "Is": cfg.Is, "k": cfg.k, "quant": cfg.quant,
+                   "parallelism": f"replicas x{args.gpus}",
+                   "l2": "no flush: the touched expert weights streamed each step exceed L2 (129 MB)",
+                   "seed": cfg.seed}
+
+    if args.impl == "reference":
+        if rank == 0:
+            line = run_reference(args, cfg, base_config, local)
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    build()
+    dev = torch.device("cuda", local)
+    inp = make_inputs(cfg, device=dev)
+    stream = torch.cuda.current_stream()
+    ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD, dev)
+    y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=dev)
+    W = B.weights_struct(inp)
+
+    def step():
+        B.forward(cfg, inp.x, W, y=y, ws=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = B.get_status(ws)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------- timed region: K steps of moe_forward
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * cfg.T * args.steps / (ms_total / 1e3)
+    launches_per_step = 11  # 2 norms, logits, select, count, scan, scatter, gather, 2 GEMMs, combine
+
+    # ---------------- the path split into its ABI calls, events around each call
+    blob = torch.empty((cfg.T, 2, cfg.k), dtype=torch.int32, device=dev)
+    ws_r = B.workspace(cfg, B.MOE_ENTRY_ROUTE, dev)
+    ws_p = B.workspace(cfg, B.MOE_ENTRY_PERMUTE, dev)
+    ws_g = B.workspace(cfg, B.MOE_ENTRY_GROUPED_GEMM, dev)
+    P = cfg.T * cfg.k
+    perm_out = (torch.empty(cfg.E, dtype=torch.int32, device=dev),
+                torch.empty(cfg.E + 1, dtype=torch.int32, device=dev),
+                torch.empty(P, dtype=torch.int32, device=dev),
+                torch.empty(P, dtype=torch.int32, device=dev))
+    xp = torch.empty((P, cfg.D), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device=dev)
+    hs = torch.empty((cfg.T, cfg.Is), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((P, cfg.D), dtype=torch.float32, device=dev)
+    os_ = torch.empty((cfg.T, cfg.D), dtype=torch.float32, device=dev)
+    y2 = torch.empty_like(y)
+    names = ["route", "permute", "gate_up", "down", "combine"]
+
+    def split_step(ev):
+        ev[0].record(stream)
+        B.route(cfg, inp.x, inp.w_router, inp.bias, blob=blob, ws=ws_r)
+        ev[1].record(stream)
+        counts, offsets, perm, inv = B.permute(cfg, blob, ws=ws_p, x=inp.x, x_perm=xp, out=perm_out)
+        ev[2].record(stream)
+        B.grouped_gemm(cfg, B.MOE_OP_GATE_UP_SWIGLU, xp, offsets, inp.w_gate_up, h,
+                       w_scales=inp.s_gate_up, a_shared=inp.x, w_shared=inp.ws_gate_up,
+                       ws_scales=inp.ss_gate_up, out_shared=hs, ws=ws_g)
+        ev[3].record(stream)
+        B.grouped_gemm(cfg, B.MOE_OP_DOWN_WEIGHTED, h, offsets, inp.w_down, o,
+                       w_scales=inp.s_down, perm_pair=perm, blob=blob, a_shared=hs,
+                       w_shared=inp.ws_down, ws_scales=inp.ss_down, out_shared=os_, ws=ws_g)
+        ev[4].record(stream)
+        B.combine(cfg, o, os_, inv, y=y2)
+        ev[5].record(stream)
+
+    ksplit = max(10, min(args.steps, 100))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(ksplit)]
+    for _ in range(3):
+        split_step(evs[0])
+    barrier()
+    for i in range(ksplit):
+        split_step(evs[i])
+    barrier()
+    per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(ksplit)) / ksplit
+           for j, n in enumerate(names)}
+    split_total = sum(evs[i][0].elapsed_time(evs[i][5]) for i in range(ksplit)) / ksplit
+    same = bool(torch.equal(y, y2))
+
+    counts = perm_out[0]
+    gu_bytes, touched = touched_gate_up_bytes(cfg, counts)
+    gu_ms = per["gate_up"]
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    traffic, traffic_src = profile_traffic()
+    roofline = {"bound": "hbm", "kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)",
+                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_source": f"{peak_src} (HBM copy, burst)",
+                "traffic": traffic, "traffic_source": traffic_src,
+                "algorithmic_bytes_per_launch": gu_bytes, "touched_experts": touched,
+                "mean_launch_ms": gu_ms}
+    lay_bytes, lay_flops = layer_bytes_flops(cfg, touched)
+    layer = {"algorithmic_bytes": lay_bytes, "algorithmic_flops": lay_flops,
+             "hbm_frac": lay_bytes / (ms_step / 1e3) / 1e9 / hbm_peak,
+             "tensor_frac": lay_flops / (ms_step / 1e3) / 1e12 / bf16_peak,
+             "binding_frac": max(lay_bytes / (hbm_peak * 1e9), lay_flops / (bf16_peak * 1e12))
+             / (ms_step / 1e3),
+             "per_call_ms": per, "split_step_ms": split_total, "split_matches_forward": same,
+             "router_refined_tokens": int(ws[4:8].view(torch.int32).item())}
+
+    # ---------------- e2e: host buffers through moe_forward_host
+    e2e = None
+    if not args.no_e2e:
+        ws_h = B.workspace(cfg, B.MOE_ENTRY_FORWARD_HOST, dev)
+        xh = inp.x.cpu().pin_memory()
+        yh = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16).pin_memory()
+        for _ in range(3):
+            B.forward_host(cfg, xh, W, yh, ws_h)
+        torch.cuda.synchronize()
+        ke = max(10, args.steps // 3)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(ke):
+            B.forward_host(cfg, xh, W, yh, ws_h)
+            stream.synchronize()  # the step's result is on the host
+        barrier()
+        dt = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([dt], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * cfg.T * ke / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": cfg.T * cfg.D * 2, "d2h_bytes_per_step": cfg.T * cfg.D * 2,
+               "ms_per_step": 1e3 * dt / ke, "steps": ke,
+               "same_output_as_device_path": bool(torch.equal(yh, y.cpu()))}
+
+    # ---------------- CPU baseline: the oracle on this host's cores (rank 0 only, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        inputs = oracle_host_inputs(inp)
+        val, cores, passes = cpu_baseline(cfg, inputs)
+        cpu = {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"the full {cfg.name} batch ({cfg.T} tokens; fp64 routing + layer) "
+                         f"x{passes} passes"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded; random-init weights of the stated shapes)",
+                "config": base_config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clk, "layer": layer,
+                "impl": "gb300"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -168,11 +168,14 @@ int moe_route(const moe_config *cfg, const void *x, const void *w_router,
  *   counts int32 [E], offsets int32 [E+1] (exclusive scan; offsets[E] = T*k),
  *   perm_pair int32 [T*k]: grouped row r holds pair perm_pair[r],
  *   inv_row int32 [T*k]:   pair p sits in grouped row inv_row[p].
+ * If x (bf16 [T][D]) and x_perm (bf16 [T*k][D]) are both non-NULL, the token
+ * rows are also gathered in grouped order: x_perm[r] = x[perm_pair[r] / k].
  * Bit-exact and deterministic.  Expert ids outside [0, E) are undefined input.
  */
 int moe_permute(const moe_config *cfg, const int32_t *blob, int32_t *counts,
                 int32_t *offsets, int32_t *perm_pair, int32_t *inv_row,
-                void *ws, size_t ws_bytes, void *stream);
+                const void *x, void *x_perm, void *ws, size_t ws_bytes,
+                void *stream);
 
 /*
  * Persistent grouped GEMM over ragged expert row groups (TMA + tcgen05/TMEM)

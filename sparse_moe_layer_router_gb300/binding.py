@@ -81,7 +81,7 @@ def lib():
             L.moe_workspace_size.argtypes = [cfgp, I]
             L.moe_workspace_size.restype = S
             L.moe_route.argtypes = [cfgp, P, P, P, P, P, S, P]
-            L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, S, P]
+            L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, P, P, S, P]
             L.moe_grouped_gemm.argtypes = [cfgp, ctypes.POINTER(MoeGemmArgs), P, S, P]
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
             L.moe_forward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
@@ -151,17 +151,22 @@ def route(cfg, x, w_router, bias=None, blob=None, ws=None, stream=None):
     return blob
 
 
-def permute(cfg, blob, ws=None, stream=None):
-    """(counts [E], offsets [E+1], perm_pair [T*k], inv_row [T*k]) int32."""
+def permute(cfg, blob, ws=None, stream=None, x=None, x_perm=None, out=None):
+    """(counts [E], offsets [E+1], perm_pair [T*k], inv_row [T*k]) int32; with ``x``
+    and ``x_perm`` also gathers token rows in grouped order.  ``out`` may hold
+    preallocated (counts, offsets, perm_pair, inv_row)."""
     dev = blob.device
-    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
-    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
-    perm = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
-    inv = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
+    if out is None:
+        out = (torch.empty(cfg.E, dtype=torch.int32, device=dev),
+               torch.empty(cfg.E + 1, dtype=torch.int32, device=dev),
+               torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev),
+               torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev))
+    counts, offsets, perm, inv = out
     if ws is None:
         ws = workspace(cfg, MOE_ENTRY_PERMUTE, dev)
     _check(lib().moe_permute(ctypes.byref(config(cfg)), _p(blob), _p(counts), _p(offsets), _p(perm),
-                             _p(inv), _p(ws), ws.numel(), _stream(stream)), "moe_permute")
+                             _p(inv), _p(x), _p(x_perm), _p(ws), ws.numel(), _stream(stream)),
+           "moe_permute")
     return counts, offsets, perm, inv
 
 

@@ -227,6 +227,15 @@ float router_gamma(const moe_config* c, const RouterPlan& rp) {
   return std::nextafter(static_cast<float>(g), INFINITY);
 }
 
+// Same for the warp-parallel fp64 re-decision: its own sum passes each product
+// through at most D/32 + 5 fp64 roundings, and the index-order definition
+// through D; the sum of both factors bounds |parallel - definition| / sum|x w|.
+double router_gamma64(const moe_config* c) {
+  const double u = std::ldexp(1.0, -53);
+  const double h1 = c->D / 32.0 + 6.0, h2 = c->D + 1.0;
+  return (h1 * u / (1.0 - h1 * u) + h2 * u / (1.0 - h2 * u)) * (1.0 + 1e-6) * 1.0001;
+}
+
 int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* wr,
                const float* bias, int32_t* blob, void* ws, const Layout& L, cudaStream_t st) {
   const RouterPlan rp = router_plan(c);
@@ -239,7 +248,8 @@ int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* w
   launch_row_norms(wr, c->E, c->D, wn, st);
   launch_router_logits(x, wr, c->T, c->D, c->E, rp.S, rp.sub_per_split, zpart, st);
   return cuda_rc(launch_router_select(zpart, rp.S, c->T, c->D, c->E, c->k, bias, xn, wn,
-                                      router_gamma(c, rp), x, wr, blob, at<int>(ws, 4), st));
+                                      router_gamma(c, rp), router_gamma64(c), x, wr, blob,
+                                      at<int>(ws, 4), st));
 }
 
 int choose_bn_max(const moe_config* c) {
@@ -416,14 +426,21 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_router, const 
 }
 
 int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int32_t* offsets,
-                int32_t* perm_pair, int32_t* inv_row, void* ws, size_t ws_bytes, void* stream) {
+                int32_t* perm_pair, int32_t* inv_row, const void* x, void* x_perm, void* ws,
+                size_t ws_bytes, void* stream) {
   if (!blob || !counts || !offsets || !perm_pair || !inv_row) return MOE_ERR_INVALID_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_ALIGN;
   DevInfo dev;
   Layout L;
   int rc = begin(cfg, MOE_ENTRY_PERMUTE, ws, ws_bytes, &dev, &L);
   if (rc) return rc;
-  return cuda_rc(launch_permute(blob, cfg->T, cfg->k, cfg->E, at<int32_t>(ws, L.chunk), counts,
-                                offsets, perm_pair, inv_row, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = cuda_rc(launch_permute(blob, cfg->T, cfg->k, cfg->E, at<int32_t>(ws, L.chunk), counts,
+                              offsets, perm_pair, inv_row, st));
+  if (rc || !x) return rc;
+  launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, x_perm, st);
+  return cuda_rc(cudaGetLastError());
 }
 
 int moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws, size_t ws_bytes,

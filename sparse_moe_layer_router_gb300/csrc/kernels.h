@@ -15,8 +15,8 @@ void launch_router_logits(const void* x, const void* wr, int T, int D, int E, in
                           int sub_per_split, float* z_part, cudaStream_t st);
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
                                  const float* bias, const float* xnorm, const float* wnorm,
-                                 float gamma, const void* x, const void* wr, int32_t* blob,
-                                 int* refine_count, cudaStream_t st);
+                                 float gamma, double gamma64, const void* x, const void* wr,
+                                 int32_t* blob, int* refine_count, cudaStream_t st);
 
 // ---- dispatch (permute.cu)
 cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,

@@ -133,28 +133,71 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 }
 
 // ---------------------------------------------------------------- select
-// The defining logit: fp64 sum in index order of exact bf16 products (+ bias).
-__device__ double exact_logit(const __nv_bfloat16* __restrict__ xr,
-                              const __nv_bfloat16* __restrict__ wrow, int D,
-                              const float* __restrict__ bias, int e) {
+// Warp-cooperative fp64 dot product of a token row and a router row: lane l
+// sums the 8-element groups l, l+32, ... in order (products are exact in
+// fp64), then a 5-level butterfly.  Each product passes through at most
+// D/32 + 5 fp64 roundings.  Every lane returns the same value (+ bias).
+__device__ double warp_dot_f64(const __nv_bfloat16* __restrict__ xr,
+                               const __nv_bfloat16* __restrict__ wrow, int D,
+                               const float* __restrict__ bias, int e, int lane) {
   double acc = 0.0;
   const uint4* xp = reinterpret_cast<const uint4*>(xr);
   const uint4* wp = reinterpret_cast<const uint4*>(wrow);
-  for (int i = 0; i < D / 8; ++i) {
-    const uint4 xv = __ldg(xp + i), wv = __ldg(wp + i);
+  for (int g = lane; g < D / 8; g += 32) {
+    const uint4 xv = __ldg(xp + g), wv = __ldg(wp + g);
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      // element 2j is the low half, 2j+1 the high half (little endian)
       acc = fma(static_cast<double>(__uint_as_float(xw[j] << 16)),
                 static_cast<double>(__uint_as_float(ww[j] << 16)), acc);
       acc = fma(static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u)),
                 static_cast<double>(__uint_as_float(ww[j] & 0xFFFF0000u)), acc);
     }
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (bias) acc += static_cast<double>(bias[e]);
   return acc;
+}
+
+// The defining logit itself: fp64 sum in index order d = 0..D-1 of the exact
+// products (+ bias last).  The warp stages 256-element chunks of both rows in
+// shared memory (`stage`: 2 x 256 bf16 per warp); lane 0 runs the chain.
+// Every lane returns the value.
+__device__ double warp_exact_logit(const __nv_bfloat16* __restrict__ xr,
+                                   const __nv_bfloat16* __restrict__ wrow, int D,
+                                   const float* __restrict__ bias, int e, int lane,
+                                   uint4* stage) {
+  double acc = 0.0;
+  const uint4* xp = reinterpret_cast<const uint4*>(xr);
+  const uint4* wp = reinterpret_cast<const uint4*>(wrow);
+  for (int c = 0; c < D / 8; c += 32) {
+    const bool in = c + lane < D / 8;
+    const uint4 xv = in ? __ldg(xp + c + lane) : make_uint4(0, 0, 0, 0);
+    const uint4 wv = in ? __ldg(wp + c + lane) : make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    stage[lane] = xv;
+    stage[32 + lane] = wv;
+    __syncwarp();
+    if (lane == 0) {
+      const int n = min(32, D / 8 - c);
+      for (int g = 0; g < n; ++g) {
+        const uint4 a = stage[g], b = stage[32 + g];
+        const uint32_t xw[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t ww[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc = fma(static_cast<double>(__uint_as_float(xw[j] << 16)),
+                    static_cast<double>(__uint_as_float(ww[j] << 16)), acc);
+          acc = fma(static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u)),
+                    static_cast<double>(__uint_as_float(ww[j] & 0xFFFF0000u)), acc);
+        }
+      }
+    }
+  }
+  if (lane == 0 && bias) acc += static_cast<double>(bias[e]);
+  return __shfl_sync(0xffffffffu, acc, 0);
 }
 
 // Order used for selection: larger value first, lower index on an exact tie.
@@ -171,12 +214,13 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ bias, const float* __restrict__ xnorm,
     const float* __restrict__ wnorm, float gamma, const __nv_bfloat16* __restrict__ x,
     const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
-    int* __restrict__ refine_count) {
-  extern __shared__ double zx_smem[];  // [8 warps][E] refined logits
+    int* __restrict__ refine_count, double gamma64) {
+  extern __shared__ double zx_smem[];  // [8 warps][E] refined logits, then [8][64] uint4 staging
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + wib;
   if (t >= T) return;
   double* zx = zx_smem + static_cast<size_t>(wib) * E;
+  uint4* stage = reinterpret_cast<uint4*>(zx_smem + static_cast<size_t>(8) * E) + wib * 64;
 
   float v[VPL], r[VPL];
   uint32_t sel = 0, cand = 0;
@@ -254,37 +298,83 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     for (int o = 16; o; o >>= 1) slots += __shfl_xor_sync(0xffffffffu, slots, o);
     if (lane == 0 && refine_count) atomicAdd(refine_count, 1);
     const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
+    // Level 2: warp-parallel fp64 logits of every candidate.
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
+      while (bal) {
+        const int src = __ffs(bal) - 1;
+        bal &= bal - 1;
+        const int e = src + 32 * i;
+        const double z = warp_dot_f64(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
+        if (lane == src) zx[e] = z;
+      }
+    }
+    __syncwarp();
+    uint32_t chosen = 0;
+    auto pick = [&](int nslots) {
+      chosen = 0;
+      for (int j = 0; j < nslots; ++j) {
+        double bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int e = lane + 32 * i;
+          if (((cand >> i) & 1u) && !((chosen >> i) & 1u) && better_d(zx[e], e, bv, be)) {
+            bv = zx[e];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (better_d(ov, oe, bv, be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+      }
+    };
+    pick(slots);
+    // Certified at fp64 level?  Radius: (parallel-sum + index-order-sum error
+    // factor) * ||x|| * ||w_e|| + 2^-52 |z| for the bias addition.
+    double lo = INFINITY, hi = -INFINITY;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      if ((cand >> i) & 1u) zx[e] = exact_logit(xr, wr + static_cast<size_t>(e) * D, D, bias, e);
+      if (!((cand >> i) & 1u)) continue;
+      const double R = gamma64 * static_cast<double>(xn) * static_cast<double>(wnorm[e]) +
+                       0x1p-52 * fabs(zx[e]);
+      if ((chosen >> i) & 1u)
+        lo = fmin(lo, zx[e] - R);
+      else
+        hi = fmax(hi, zx[e] + R);
     }
-    __syncwarp();
-    sel &= ~cand;  // candidates compete for the remaining slots on exact values
-    uint32_t chosen = 0;
-    for (int j = 0; j < slots; ++j) {
-      double bv = -INFINITY;
-      int be = 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      lo = fmin(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmax(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (!(lo > hi)) {
+      // Level 3: the defining index-order fp64 sum (exact ties end here).
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        if (((cand >> i) & 1u) && !((chosen >> i) & 1u) && better_d(zx[e], e, bv, be)) {
-          bv = zx[e];
-          be = e;
+        uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
+        while (bal) {
+          const int src = __ffs(bal) - 1;
+          bal &= bal - 1;
+          const int e = src + 32 * i;
+          const double z =
+              warp_exact_logit(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane, stage);
+          if (lane == src) zx[e] = z;
         }
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better_d(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+      __syncwarp();
+      pick(slots);
     }
-    sel |= chosen;
+    sel = (sel & ~cand) | chosen;
     // Refined logits replace the fp32 ones for the weights.
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
@@ -345,10 +435,10 @@ void launch_router_logits(const void* x, const void* wr, int T, int D, int E, in
 
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
                                  const float* bias, const float* xnorm, const float* wnorm,
-                                 float gamma, const void* x, const void* wr, int32_t* blob,
-                                 int* refine_count, cudaStream_t st) {
+                                 float gamma, double gamma64, const void* x, const void* wr,
+                                 int32_t* blob, int* refine_count, cudaStream_t st) {
   const int blocks = (T + 7) / 8;
-  const size_t smem = static_cast<size_t>(8) * E * sizeof(double);
+  const size_t smem = static_cast<size_t>(8) * E * sizeof(double) + 8 * 64 * sizeof(uint4);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const auto* wb = static_cast<const __nv_bfloat16*>(wr);
 #define MOE_SELECT_CASE(V)                                                                   \
@@ -361,7 +451,7 @@ cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E
     }                                                                                        \
     router_select_kernel<V><<<blocks, 256, smem, st>>>(z_part, S, T, D, E, k, bias, xnorm,   \
                                                        wnorm, gamma, xb, wb, blob,           \
-                                                       refine_count);                        \
+                                                       refine_count, gamma64);               \
     return cudaGetLastError();                                                               \
   }
   MOE_SELECT_CASE(1)

@@ -62,6 +62,9 @@ CONFIGS = {
                         zipf_s=1.2, zipf_alpha=0.9492),
     "w4a16": MoEConfig("w4a16", T=1024, D=4096, E=512, I=1024, Is=1024, k=10, quant=1,
                        group=128),
+    # Same per-expert shapes as "decode" with 64 experts (1.6 GB of weights): the
+    # case the detailed hardware-counter captures run on.
+    "decode_e64": MoEConfig("decode_e64", T=64, D=4096, E=64, I=1024, Is=1024, k=10),
 }
 
 _TAG_X, _TAG_WR, _TAG_RANK = 1, 2, 3

@@ -74,7 +74,8 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.moe_route(ctypes.byref(cfg), None, d, None, d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
     odd = ctypes.c_void_p(4096 + 2)
     assert lib.moe_route(ctypes.byref(cfg), odd, d, None, d, d, 1 << 30, None) == B.MOE_ERR_ALIGN
-    assert lib.moe_permute(ctypes.byref(cfg), None, d, d, d, d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(ctypes.byref(cfg), None, d, d, d, d, None, None, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(ctypes.byref(cfg), d, d, d, d, d, d, None, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
     w = B.MoeWeights()
     assert lib.moe_forward(ctypes.byref(cfg), d, ctypes.byref(w), d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
     args = B.MoeGemmArgs()
