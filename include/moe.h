@@ -60,6 +60,7 @@ extern "C" {
 #define MOE_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed           */
 #define MOE_ERR_TIMEOUT (-5)      /* a device wait hit its bound (moe_get_status)   */
 #define MOE_ERR_ALIGN (-6)        /* a pointer is not 16-byte aligned               */
+#define MOE_ERR_SCRATCH_LIMIT (-7) /* too large for moe_permute_static's fixed scratch */
 
 /* ---- weight formats ---- */
 #define MOE_QUANT_BF16 0    /* bf16 expert weights                                   */
@@ -176,6 +177,34 @@ int moe_permute(const moe_config *cfg, const int32_t *blob, int32_t *counts,
                 int32_t *offsets, int32_t *perm_pair, int32_t *inv_row,
                 const void *x, void *x_perm, void *ws, size_t ws_bytes,
                 void *stream);
+
+/*
+ * moe_permute_static: moe_permute for callers that cannot allocate device
+ * memory.  (This entry point has no counterpart in the pages; it is an
+ * interface convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc or hand the library a workspace: a
+ * plug-in or foreign-language caller that holds only the tensors it was given,
+ * an engine whose device memory is owned by an allocator this call site cannot
+ * reach, or a serving loop that must not allocate once it is running.  This
+ * variant needs no workspace: its scratch (the per-chunk expert count table)
+ * is a fixed array inside the library, 65536 int32 (256 KiB), kept in every
+ * GPU that loads the library until the process exits.  The call allocates
+ * nothing and calls no allocating routine.
+ *   Same arguments and results as moe_permute, bit for bit, without ws.
+ *   Limit: ceil(T*k / 2048) * E <= 65536 (e.g. E = 512: T*k <= 262144);
+ *   larger problems return MOE_ERR_SCRATCH_LIMIT and launch nothing.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   All calls share the one array: calls that may overlap on the GPU (other
+ *   streams, other host threads) race and must be serialised by the caller.
+ *   Each call writes every table entry it reads, so no clearing is needed.
+ */
+int moe_permute_static(const moe_config *cfg, const int32_t *blob,
+                       int32_t *counts, int32_t *offsets, int32_t *perm_pair,
+                       int32_t *inv_row, const void *x, void *x_perm,
+                       void *stream);
 
 /*
  * Persistent grouped GEMM over ragged expert row groups (TMA + tcgen05/TMEM)

@@ -23,6 +23,7 @@ MOE_ERR_WORKSPACE = -3
 MOE_ERR_CUDA = -4
 MOE_ERR_TIMEOUT = -5
 MOE_ERR_ALIGN = -6
+MOE_ERR_SCRATCH_LIMIT = -7
 
 MOE_QUANT_BF16 = 0
 MOE_QUANT_W4A16 = 1
@@ -35,8 +36,9 @@ MOE_ENTRY_FORWARD = 3
 MOE_ENTRY_FORWARD_HOST = 4
 
 # Every function declared in include/moe.h.
-EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_gemm", "moe_combine",
-           "moe_forward", "moe_forward_host", "moe_get_status", "moe_strerror")
+EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_static",
+           "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status",
+           "moe_strerror")
 
 
 class MoeError(RuntimeError):
@@ -82,6 +84,7 @@ def lib():
             L.moe_workspace_size.restype = S
             L.moe_route.argtypes = [cfgp, P, P, P, P, P, S, P]
             L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, P, P, S, P]
+            L.moe_permute_static.argtypes = [cfgp, P, P, P, P, P, P, P, P]
             L.moe_grouped_gemm.argtypes = [cfgp, ctypes.POINTER(MoeGemmArgs), P, S, P]
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
             L.moe_forward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
@@ -89,8 +92,8 @@ def lib():
             L.moe_get_status.argtypes = [P, P]
             L.moe_strerror.argtypes = [I]
             L.moe_strerror.restype = ctypes.c_char_p
-            for n in ("moe_route", "moe_permute", "moe_grouped_gemm", "moe_combine", "moe_forward",
-                      "moe_forward_host", "moe_get_status"):
+            for n in ("moe_route", "moe_permute", "moe_permute_static", "moe_grouped_gemm",
+                      "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status"):
                 getattr(L, n).restype = I
             _lib = L
     return _lib
@@ -167,6 +170,19 @@ def permute(cfg, blob, ws=None, stream=None, x=None, x_perm=None, out=None):
     _check(lib().moe_permute(ctypes.byref(config(cfg)), _p(blob), _p(counts), _p(offsets), _p(perm),
                              _p(inv), _p(x), _p(x_perm), _p(ws), ws.numel(), _stream(stream)),
            "moe_permute")
+    return counts, offsets, perm, inv
+
+
+def permute_static(cfg, blob, stream=None, x=None, x_perm=None):
+    """moe_permute without a workspace (fixed scratch inside the library)."""
+    dev = blob.device
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
+    inv = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
+    _check(lib().moe_permute_static(ctypes.byref(config(cfg)), _p(blob), _p(counts), _p(offsets),
+                                    _p(perm), _p(inv), _p(x), _p(x_perm), _stream(stream)),
+           "moe_permute_static")
     return counts, offsets, perm, inv
 
 

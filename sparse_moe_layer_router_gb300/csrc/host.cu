@@ -443,6 +443,25 @@ int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int
   return cuda_rc(cudaGetLastError());
 }
 
+int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* counts,
+                       int32_t* offsets, int32_t* perm_pair, int32_t* inv_row, const void* x,
+                       void* x_perm, void* stream) {
+  int rc = validate(cfg);
+  if (rc) return rc;
+  if (!blob || !counts || !offsets || !perm_pair || !inv_row) return MOE_ERR_INVALID_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_ALIGN;
+  const long P = static_cast<long>(cfg->T) * cfg->k;
+  const long chunks = (P + kPermuteChunk - 1) / kPermuteChunk;
+  if (chunks * cfg->E > kStaticPermuteScratchInts) return MOE_ERR_SCRATCH_LIMIT;
+  DevInfo dev;
+  rc = current_device(&dev);
+  if (rc) return rc;
+  return cuda_rc(launch_permute_static(blob, cfg->T, cfg->k, cfg->E, counts, offsets, perm_pair,
+                                       inv_row, x, cfg->D, x_perm,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 int moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws, size_t ws_bytes,
                      void* stream) {
   int rc = validate(cfg);
@@ -531,6 +550,8 @@ const char* moe_strerror(int code) {
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MOE_ERR_SCRATCH_LIMIT:
+      return "problem larger than the fixed scratch of moe_permute_static";
     default: return "unknown error";
   }
 }

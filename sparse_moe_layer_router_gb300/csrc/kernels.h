@@ -24,6 +24,11 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
                            int32_t* inv_row, cudaStream_t st);
 void launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div, void* out,
                         cudaStream_t st);
+// Capacity (int32 entries) of the fixed device array behind moe_permute_static.
+constexpr long kStaticPermuteScratchInts = 65536;
+cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int32_t* counts,
+                                  int32_t* offsets, int32_t* perm_pair, int32_t* inv_row,
+                                  const void* x, int D, void* x_perm, cudaStream_t st);
 
 // ---- combine (combine.cu)
 void launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T, int D,

@@ -11,6 +11,8 @@
 // positions plus counts/offsets (scan kernel), and each chunk places its pairs
 // in order (scatter kernel: per-warp segments, __match_any_sync for ranks
 // within a step of 32).
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -167,6 +169,51 @@ void launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int 
                         cudaStream_t st) {
   gather_rows_kernel<<<rows, 256, 0, st>>>(static_cast<const uint4*>(a), idx, rows, D / 8, div,
                                            static_cast<uint4*>(out));
+}
+
+// ------------------------------------------------------------------
+// Fixed scratch for moe_permute_static: the [chunks][E] count table lives in
+// this file-scope device array (kStaticPermuteScratchInts int32 = 256 KiB)
+// instead of a caller-provided workspace.  Every device that loads the
+// library holds it until the process exits.  Each call overwrites the entries
+// it uses before reading them, so nothing needs clearing; calls that overlap
+// on the GPU share the array and race.
+static __device__ __align__(256) int32_t g_permute_scratch[kStaticPermuteScratchInts];
+
+namespace {
+std::mutex g_scratch_mu;
+int32_t* g_scratch_addr[64] = {};
+}  // namespace
+
+// Device address of g_permute_scratch on the current device.  In host code the
+// symbol names a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+static cudaError_t static_scratch(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int32_t* counts,
+                                  int32_t* offsets, int32_t* perm_pair, int32_t* inv_row,
+                                  const void* x, int D, void* x_perm, cudaStream_t st) {
+  int32_t* table = nullptr;
+  cudaError_t e = static_scratch(&table);
+  if (e != cudaSuccess) return e;
+  e = launch_permute(blob, T, k, E, table, counts, offsets, perm_pair, inv_row, st);
+  if (e != cudaSuccess || !x) return e;
+  launch_gather_rows(x, perm_pair, T * k, D, k, x_perm, st);
+  return cudaGetLastError();
 }
 
 }  // namespace moe
