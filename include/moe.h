@@ -245,6 +245,17 @@ int moe_forward_host(const moe_config *cfg, const void *x_host,
  */
 int moe_get_status(void *ws, void *stream);
 
+/*
+ * Self-test of the device-side timeout path: launches one CTA that holds
+ * tensor memory, waits on a barrier that nothing ever completes, gives up after
+ * `limit_ms` (1 .. 10000), records MOE_ERR_TIMEOUT in the status word of `ws`
+ * (>= 256 bytes), frees the tensor memory and exits.  moe_get_status(ws, ...)
+ * then returns MOE_ERR_TIMEOUT and the context stays usable.  This is the same
+ * bounded-wait code every pipelined kernel of the library uses.
+ */
+int moe_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned int limit_ms,
+                              void *stream);
+
 /* Static description of an error code. */
 const char *moe_strerror(int code);
 

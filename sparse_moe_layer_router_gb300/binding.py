@@ -38,7 +38,7 @@ MOE_ENTRY_FORWARD_HOST = 4
 # Every function declared in include/moe.h.
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_static",
            "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status",
-           "moe_strerror")
+           "moe_selftest_wait_timeout", "moe_strerror")
 
 
 class MoeError(RuntimeError):
@@ -90,10 +90,12 @@ def lib():
             L.moe_forward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
             L.moe_forward_host.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
             L.moe_get_status.argtypes = [P, P]
+            L.moe_selftest_wait_timeout.argtypes = [P, S, ctypes.c_uint, P]
             L.moe_strerror.argtypes = [I]
             L.moe_strerror.restype = ctypes.c_char_p
             for n in ("moe_route", "moe_permute", "moe_permute_static", "moe_grouped_gemm",
-                      "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status"):
+                      "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status",
+                      "moe_selftest_wait_timeout"):
                 getattr(L, n).restype = I
             _lib = L
     return _lib
@@ -243,3 +245,10 @@ def forward_host(cfg, x_host, weights, y_host, ws, stream=None):
 
 def get_status(ws, stream=None) -> int:
     return int(lib().moe_get_status(_p(ws), _stream(stream)))
+
+
+def selftest_wait_timeout(ws, limit_ms=200, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the device status it leaves (MOE_ERR_TIMEOUT)."""
+    _check(lib().moe_selftest_wait_timeout(_p(ws), ws.numel(), int(limit_ms), _stream(stream)),
+           "moe_selftest_wait_timeout")
+    return get_status(ws, stream)

@@ -48,4 +48,38 @@ void launch_combine(const float* o, const float* o_shared, const int32_t* inv_ro
                                        k, static_cast<uint2*>(y));
 }
 
+// ------------------------------------------------------------------
+// Self-test of the bounded-wait path every pipelined kernel relies on: one CTA
+// holds TMEM, waits on an mbarrier that nothing arrives on, gives up after
+// `limit_ns`, records MOE_ERR_TIMEOUT in the status word, frees TMEM and exits.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(int* status,
+                                                           unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  tmem_alloc(&tmem, 32);
+  tmem_relinquish();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag, limit_ns)) {
+    abort_flag = 1;
+    atomicCAS(status, 0, MOE_ERR_TIMEOUT);
+  }
+  __syncthreads();
+  __syncwarp();
+  tc_fence_after();
+  tmem_dealloc(tmem, 32);
+}
+
+cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -35,16 +35,25 @@ namespace moe {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kAStage = kBM * kBK * 2;  // 16 KB
+constexpr int kAStage = kBM * kBK * 2;      // 16 KB bf16 operand tile
+constexpr int kARawStage = kBM * kBK / 2;   // 4 KB packed int4 tile
 constexpr int kMaxGroups = 1025;
-constexpr int kGemmThreads = 192;
+constexpr int kDequantWarps = 8;
 
-template <int BN_MAX, int STAGES>
+template <int QUANT>
+struct GemmRoles {
+  static constexpr int kThreads = QUANT ? 192 + 32 * kDequantWarps : 192;
+  static constexpr int kEmptyArrivals = QUANT ? 1 + kDequantWarps : 1;
+};
+
+template <int BN_MAX, int STAGES, int QUANT>
 struct GemmSmem {
-  uint8_t a[STAGES][kAStage];
-  uint8_t b[STAGES][BN_MAX * 128];
+  uint8_t a[STAGES][kAStage];                             // bf16 operand, 128-B swizzle
+  uint8_t b[STAGES][BN_MAX * 128];                        // token rows, 128-B swizzle
+  uint8_t araw[QUANT ? STAGES : 1][QUANT ? kARawStage : 16];  // packed int4 rows (W4A16)
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
+  uint64_t aready[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -89,9 +98,8 @@ __device__ __forceinline__ void record_error(const GemmParams& p, volatile int* 
   if (p.status) atomicCAS(p.status, 0, code);
 }
 
-template <int BN_MAX, int STAGES>
-__device__ __forceinline__ TileInfo decode_tile(const GemmSmem<BN_MAX, STAGES>& s,
-                                                const GemmParams& p, int G, int L) {
+template <typename Smem, int BN_MAX>
+__device__ __forceinline__ TileInfo decode_tile(const Smem& s, const GemmParams& p, int G, int L) {
   int lo = 0, hi = G;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -118,17 +126,56 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmSmem<BN_MAX, STAGES>& 
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int BN_MAX, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a,
-                             const __grid_constant__ CUtensorMap tm_a_s,
-                             const __grid_constant__ CUtensorMap tm_b,
-                             const __grid_constant__ CUtensorMap tm_b_s, const GemmParams p) {
+// Weight row (in the full weight matrix of its group) held by row r of a tile.
+// Gate/up tiles hold four blocks of (16 gate rows, 16 up rows) of features
+// m*64 .. m*64+63; down tiles hold rows m*128 .. m*128+127.
+__device__ __forceinline__ int tile_weight_row(const GemmParams& p, const TileInfo& t, int r) {
+  if (p.op == kOpGateUp) {
+    const int half = t.shared ? p.ld_out_s : p.ld_out;  // I of the group
+    const int b = r >> 5, j = r & 31;
+    const int f = t.m * 64 + 16 * b + (j & 15);
+    const int base = t.shared ? 0 : t.e * p.a_rows_per_expert;
+    return base + (j < 16 ? f : half + f);
+  }
+  return (t.shared ? 0 : t.e * p.a_rows_per_expert) + t.m * kBM + r;
+}
+
+// Eight signed 4-bit values (value j in bits 4j..4j+3) times a bf16 scale ->
+// eight bf16 in order, each bf16_rne(q * s).  Nibbles become offset binary
+// (q + 8), are placed in the mantissa of 128.0 (0x4300 | u = 128 + u, exact),
+// shifted back by 136 (exact) and multiplied by the scale (one rounding).
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
+  const uint32_t x = w ^ 0x88888888u;
+  const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
+  uint32_t h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = ((x >> (4 * i)) & 0x000F000Fu) | 0x43004300u;  // (e_i, e_{i+4})
+    __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t), k136);
+    __nv_bfloat162 v = __hmul2(q, s2);
+    h[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  uint4 out;
+  out.x = __byte_perm(h[0], h[1], 0x5410);  // e0, e1
+  out.y = __byte_perm(h[2], h[3], 0x5410);  // e2, e3
+  out.z = __byte_perm(h[0], h[1], 0x7632);  // e4, e5
+  out.w = __byte_perm(h[2], h[3], 0x7632);  // e6, e7
+  return out;
+}
+
+template <int BN_MAX, int STAGES, int QUANT>
+__global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                        const __grid_constant__ CUtensorMap tm_a_s,
+                        const __grid_constant__ CUtensorMap tm_b,
+                        const __grid_constant__ CUtensorMap tm_b_s, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  using Smem = GemmSmem<BN_MAX, STAGES>;
+  using Smem = GemmSmem<BN_MAX, STAGES, QUANT>;
+  constexpr int kThreads = GemmRoles<QUANT>::kThreads;
   const uint32_t raw = smem_u32(smem_raw);
   Smem& s = *reinterpret_cast<Smem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
   constexpr uint32_t kTmemCols = (2 * BN_MAX < 32) ? 32u : static_cast<uint32_t>(2 * BN_MAX);
+  constexpr uint32_t kABytes = QUANT ? kARawStage : kAStage;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.E + p.has_shared;
@@ -136,7 +183,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1);
+      mbar_init(&s.empty[i], GemmRoles<QUANT>::kEmptyArrivals);
+      mbar_init(&s.aready[i], kDequantWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -154,10 +202,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       prefetch_tmap(&tm_b_s);
     }
   }
-  for (int i = threadIdx.x; i <= p.E; i += kGemmThreads) s.off[i] = p.offsets[i];
+  for (int i = threadIdx.x; i <= p.E; i += kThreads) s.off[i] = p.offsets[i];
   __syncthreads();
   // Tiles per group, then an exclusive scan into tile_start.
-  for (int g = threadIdx.x; g < G; g += kGemmThreads) {
+  for (int g = threadIdx.x; g < G; g += kThreads) {
     const bool sh = p.has_shared && g == 0;
     const int e = g - p.has_shared;
     const int rows = sh ? p.T_shared : s.off[e + 1] - s.off[e];
@@ -200,14 +248,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued = 0;  // bit i: stage i has a load in flight or done, phase in issued_ph
+      uint32_t issued = 0;  // bit i: stage i had a load issued; its phase in issued_ph
       uint32_t issued_ph = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-        const TileInfo t = decode_tile(s, p, G, L);
+        const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
         const CUtensorMap* ma = t.shared ? &tm_a_s : &tm_a;
         const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
-        const uint32_t bytes = kAStage + static_cast<uint32_t>(t.bn) * 128u;
+        const uint32_t bytes = kABytes + static_cast<uint32_t>(t.bn) * 128u;
         const int a_row0 = t.shared ? 0 : t.e * p.a_rows_per_expert;
         for (int kb = 0; kb < t.k_blocks; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
@@ -218,13 +266,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           issued |= 1u << stage;
           issued_ph = (issued_ph & ~(1u << stage)) | (phase << stage);
           const int kc = kb * kBK;
+          // weights: bf16 tiles at column kc, or packed int4 at word kc / 8
+          void* adst = QUANT ? static_cast<void*>(s.araw[stage]) : static_cast<void*>(s.a[stage]);
+          const int ac = QUANT ? kc / 8 : kc;
+          constexpr int kRowBytes = QUANT ? kBK / 2 : kBK * 2;
           if (p.op == kOpGateUp) {
             const int row = a_row0 + t.m * 64;
 #pragma unroll
             for (int b = 0; b < 4; ++b)
-              tma_load_3d(s.a[stage] + b * 4096, ma, &s.full[stage], kc, row + 16 * b, 0, pol_w);
+              tma_load_3d(static_cast<uint8_t*>(adst) + b * 32 * kRowBytes, ma, &s.full[stage], ac,
+                          row + 16 * b, 0, pol_w);
           } else {
-            tma_load_2d(s.a[stage], ma, &s.full[stage], kc, a_row0 + t.m * kBM, pol_w);
+            tma_load_2d(adst, ma, &s.full[stage], ac, a_row0 + t.m * kBM, pol_w);
           }
           for (int i = 0; i < t.bn / 16; ++i)
             tma_load_2d(s.b[stage] + i * 2048, mb, &s.full[stage], kc, t.b_row + 16 * i, pol_x);
@@ -249,7 +302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-        const TileInfo t = decode_tile(s, p, G, L);
+        const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
         if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -258,7 +311,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN_MAX);
         const uint32_t idesc = idesc_bf16_f32(kBM, t.bn);
         for (int kb = 0; kb < t.k_blocks; ++kb) {
-          if (!mbar_wait(&s.full[stage], phase, abort_flag)) {
+          if ((QUANT && !mbar_wait(&s.aready[stage], phase, abort_flag)) ||
+              !mbar_wait(&s.full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -284,13 +338,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mma_commit(&s.drain);
       mbar_wait_time_only(&s.drain, 0);
     }
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------------- epilogue (warps 2-5)
     const int sp = warp & 3;  // TMEM lanes 32*sp .. 32*sp+31
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int L = blockIdx.x; L < ntiles; L += gridDim.x) {
-      const TileInfo t = decode_tile(s, p, G, L);
+      const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
       if (!mbar_wait(&s.tfull[acc], acc_phase, abort_flag)) {
         record_error(p, abort_flag, MOE_ERR_TIMEOUT);
         break;
@@ -353,32 +407,82 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+  } else if (QUANT) {
+    // -------------------------------------------------- dequant (warps 6-13, W4A16)
+    // Thread -> (tile row r, half of its 8 packed words).  Reads 16 B of packed
+    // int4, writes four 16-B chunks of bf16 into the 128-B-swizzled operand
+    // tile: chunk c of row r lives at r*128 + ((c ^ (r & 7)) << 4).
+    const int td = (warp - 6) * 32 + lane;
+    const int r = td >> 1, half = td & 1;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+      const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
+      const int K = t.shared ? p.K_s : p.K;
+      const uint16_t* srow = (t.shared ? p.wscale_s : p.wscale) +
+                             static_cast<size_t>(tile_weight_row(p, t, r)) * (K / p.group);
+      for (int kb = 0; kb < t.k_blocks; ++kb) {
+        const uint16_t sbits = __ldg(srow + (kb * kBK) / p.group);
+        __nv_bfloat162 s2;
+        s2.x = __ushort_as_bfloat16(sbits);
+        s2.y = s2.x;
+        if (!mbar_wait(&s.full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint4 pk = *reinterpret_cast<const uint4*>(s.araw[stage] + r * 32 + half * 16);
+        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
+        uint8_t* arow = s.a[stage] + r * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = half * 4 + i;
+          *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(words[i], s2);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s.aready[stage]);
+          mbar_arrive(&s.empty[stage]);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
   }
 
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <int BN_MAX, int STAGES>
-static cudaError_t launch_bf16(const GemmParams& p, const GemmMaps& m, int num_sms,
-                               cudaStream_t st) {
-  const size_t smem = sizeof(GemmSmem<BN_MAX, STAGES>) + 1024;
-  auto kern = grouped_gemm_bf16_kernel<BN_MAX, STAGES>;
+template <int BN_MAX, int STAGES, int QUANT>
+static cudaError_t launch_variant(const GemmParams& p, const GemmMaps& m, int num_sms,
+                                  cudaStream_t st) {
+  const size_t smem = sizeof(GemmSmem<BN_MAX, STAGES, QUANT>) + 1024;
+  auto kern = grouped_gemm_kernel<BN_MAX, STAGES, QUANT>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kGemmThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, p);
+  kern<<<num_sms, GemmRoles<QUANT>::kThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int bn_max, int quant,
                                 int num_sms, cudaStream_t st) {
-  if (quant != 0) return cudaErrorNotSupported;
-  if (bn_max == 64) return launch_bf16<64, 8>(p, maps, num_sms, st);
-  if (bn_max == 256) return launch_bf16<256, 4>(p, maps, num_sms, st);
+  if (quant == 0) {
+    if (bn_max == 64) return launch_variant<64, 8, 0>(p, maps, num_sms, st);
+    if (bn_max == 256) return launch_variant<256, 4, 0>(p, maps, num_sms, st);
+  } else if (quant == 1) {
+    if (bn_max == 64) return launch_variant<64, 7, 1>(p, maps, num_sms, st);
+    if (bn_max == 256) return launch_variant<256, 4, 1>(p, maps, num_sms, st);
+  }
   return cudaErrorInvalidValue;
 }
 

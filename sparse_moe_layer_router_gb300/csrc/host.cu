@@ -105,6 +105,35 @@ bool map_gate_up_bf16(CUtensorMap* m, const void* base, uint64_t groups, uint64_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed int4 weights [rows][cols/8] int32 (no swizzle): 2-D map with a
+// {8 words = 64 values, box_rows} box.
+bool map_2d_i4(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols / 8, rows};
+  const cuuint64_t strides[1] = {cols / 2};
+  const cuuint32_t box[2] = {8, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Packed int4 gate/up weights [groups][2*half][cols/8]: the 3-D gate/up pairing
+// of map_gate_up_bf16 with a {8 words, 16, 2} box.
+bool map_gate_up_i4(CUtensorMap* m, const void* base, uint64_t groups, uint64_t half,
+                    uint64_t cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {cols / 8, groups * 2 * half, 2};
+  const cuuint64_t strides[2] = {cols / 2, half * (cols / 2)};
+  const cuuint32_t box[3] = {8, 16, 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- validation
 int validate(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
@@ -262,7 +291,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   const int P = c->T * c->k;
   const bool gate_up = a->op == MOE_OP_GATE_UP_SWIGLU;
   const bool has_shared = a->a_shared != nullptr;
-  if (c->quant != MOE_QUANT_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool w4 = c->quant == MOE_QUANT_W4A16;
   const void* b_routed = a->a;
   if (a->a_row_index) {
     if (!gate_up) return MOE_ERR_INVALID_ARG;
@@ -283,6 +312,11 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   p.status = at<int>(ws, 0);
   p.out = a->out;
   p.out_s = a->out_shared;
+  p.wscale = static_cast<const uint16_t*>(a->w_scales);
+  p.wscale_s = static_cast<const uint16_t*>(a->ws_scales);
+  p.K = gate_up ? c->D : c->I;
+  p.K_s = gate_up ? c->D : c->I_shared;
+  p.group = w4 ? c->group : 128;
   bool ok = true;
   if (gate_up) {
     p.m_tiles = c->I / 64;
@@ -291,10 +325,12 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     p.a_rows_per_expert = 2 * c->I;
     p.ld_out = c->I;
     p.ld_out_s = c->I_shared;
-    ok &= map_gate_up_bf16(&maps.a, a->w, c->E, c->I, c->D);
+    ok &= w4 ? map_gate_up_i4(&maps.a, a->w, c->E, c->I, c->D)
+             : map_gate_up_bf16(&maps.a, a->w, c->E, c->I, c->D);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, 16);
     if (has_shared) {
-      ok &= map_gate_up_bf16(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
+      ok &= w4 ? map_gate_up_i4(&maps.a_s, a->w_shared, 1, c->I_shared, c->D)
+               : map_gate_up_bf16(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->D, 16);
     }
   } else {
@@ -305,10 +341,12 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     p.a_rows_per_expert = c->D;
     p.ld_out = c->D;
     p.ld_out_s = c->D;
-    ok &= map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128);
+    ok &= w4 ? map_2d_i4(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128)
+             : map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, 16);
     if (has_shared) {
-      ok &= map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
+      ok &= w4 ? map_2d_i4(&maps.a_s, a->w_shared, c->D, c->I_shared, 128)
+               : map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, 16);
     }
   }
@@ -539,6 +577,18 @@ int moe_get_status(void* ws, void* stream) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (h != 0 && cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
   return h;
+}
+
+int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned int limit_ms, void* stream) {
+  if (!ws || ws_bytes < kHeader) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_ALIGN;
+  if (limit_ms < 1 || limit_ms > 10000) return MOE_ERR_INVALID_ARG;
+  DevInfo dev;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_rc(launch_selftest_wait(at<int>(ws, 0), 1000000ull * limit_ms, st));
 }
 
 const char* moe_strerror(int code) {

@@ -34,6 +34,9 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
 void launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T, int D,
                     int k, void* y, cudaStream_t st);
 
+// ---- bounded-wait self-test (combine.cu)
+cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
+
 // ---- grouped GEMM (grouped_gemm.cu)
 enum GemmOp : int { kOpGateUp = 0, kOpDown = 1 };
 

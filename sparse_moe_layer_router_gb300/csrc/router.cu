@@ -143,6 +143,7 @@ __device__ double warp_dot_f64(const __nv_bfloat16* __restrict__ xr,
   double acc = 0.0;
   const uint4* xp = reinterpret_cast<const uint4*>(xr);
   const uint4* wp = reinterpret_cast<const uint4*>(wrow);
+#pragma unroll 4
   for (int g = lane; g < D / 8; g += 32) {
     const uint4 xv = __ldg(xp + g), wv = __ldg(wp + g);
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -225,15 +226,27 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   float v[VPL], r[VPL];
   uint32_t sel = 0, cand = 0;
   const float xn = xnorm[t];
+  // Split-K partials summed in split order; the VPL loads of one split are
+  // independent (and coalesced across the warp), so they are issued together.
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) v[i] = 0.f;
+  for (int sp = 0; sp < S; ++sp) {
+    const float* zp = z_part + (static_cast<size_t>(sp) * T + t) * E;
+    float part[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      part[i] = e < E ? __ldg(zp + e) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] += part[i];
+  }
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      float s = 0.f;
-      for (int sp = 0; sp < S; ++sp) s += z_part[(static_cast<size_t>(sp) * T + t) * E + e];
-      if (bias) s += bias[e];
-      v[i] = s;
-      r[i] = gamma * xn * wnorm[e] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(s);
+      if (bias) v[i] += __ldg(bias + e);
+      r[i] = gamma * xn * __ldg(wnorm + e) * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]);
     } else {
       v[i] = -INFINITY;
       r[i] = 0.f;
