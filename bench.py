@@ -416,7 +416,8 @@ def main():
              "binding_frac": max(lay_bytes / (hbm_peak * 1e9), lay_flops / (bf16_peak * 1e12))
              / (ms_step / 1e3),
              "per_call_ms": per, "split_step_ms": split_total, "split_matches_forward": same,
-             "router_refined_tokens": int(ws[4:8].view(torch.int32).item())}
+             "router_refined_tokens": int(ws[4:8].view(torch.int32).item()),
+             "router_exact_fallback_tokens": int(ws[8:12].view(torch.int32).item())}
 
     # ---------------- e2e: host buffers through moe_forward_host
     e2e = None

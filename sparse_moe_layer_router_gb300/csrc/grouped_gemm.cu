@@ -61,6 +61,7 @@ struct GemmSmem {
   int abort_flag;
   int tile_start[kMaxGroups + 1];
   int off[kMaxGroups];
+  float row_weight[4][BN_MAX];  // down epilogue: routing weight of each token row, per warp
 };
 
 struct TileInfo {
@@ -341,10 +342,28 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
   } else if (warp < 6) {
     // -------------------------------------------------- epilogue (warps 2-5)
     const int sp = warp & 3;  // TMEM lanes 32*sp .. 32*sp+31
+    float* wts = s.row_weight[warp - 2];
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int L = blockIdx.x; L < ntiles; L += gridDim.x) {
       const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
+      if (p.op == kOpDown) {
+        // Routing weight of every token row of the tile, fetched before the
+        // accumulator is ready: row r holds pair p = perm_pair[r] (token p / k,
+        // slot p % k); the shared group has weight 1.
+        __syncwarp();
+        for (int j = lane; j < t.n_valid; j += 32) {
+          float wgt = 1.0f;
+          if (!t.shared) {
+            const int pr = __ldg(p.perm_pair + t.b_row + j);
+            const int tk = pr / p.k;
+            wgt = __int_as_float(
+                __ldg(p.blob + static_cast<size_t>(tk) * 2 * p.k + p.k + (pr - tk * p.k)));
+          }
+          wts[j] = wgt;
+        }
+        __syncwarp();
+      }
       if (!mbar_wait(&s.tfull[acc], acc_phase, abort_flag)) {
         record_error(p, abort_flag, MOE_ERR_TIMEOUT);
         break;
@@ -387,17 +406,8 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int col = c0 + i;
-            if (col < t.n_valid) {
-              const int row = t.b_row + col;
-              float wgt = 1.0f;
-              if (!t.shared) {
-                const int pr = __ldg(p.perm_pair + row);
-                const int tk = pr / p.k;
-                wgt = __int_as_float(
-                    __ldg(p.blob + static_cast<size_t>(tk) * 2 * p.k + p.k + (pr - tk * p.k)));
-              }
-              out[static_cast<size_t>(row) * ld + f] = wgt * __uint_as_float(r[i]);
-            }
+            if (col < t.n_valid)
+              out[static_cast<size_t>(t.b_row + col) * ld + f] = wts[col] * __uint_as_float(r[i]);
           }
         }
       }

@@ -19,7 +19,9 @@ namespace {
 
 using namespace moe;
 
-constexpr size_t kHeader = 256;  // status word (int32 at 0), refine counter (int32 at 4)
+// Workspace header: status word (int32 at 0); router counters (int32 at 4:
+// tokens re-decided at level 2, at 8: tokens that needed level 3).
+constexpr size_t kHeader = 256;
 constexpr int kRouterTargetCtas = 304;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -199,8 +201,8 @@ Layout layout(const moe_config* c, int entry) {
   const size_t chunks = (P + kPermuteChunk - 1) / kPermuteChunk;
   auto route_part = [&] {
     L.zpart = cv.take(static_cast<size_t>(rp.S) * T * E * 4);
-    L.xnorm = cv.take(T * 4);
-    L.wnorm = cv.take(E * 4);
+    L.xnorm = cv.take(static_cast<size_t>(rp.S) * T * 4);  // split partial sums of squares
+    L.wnorm = cv.take(static_cast<size_t>(rp.S) * E * 4);
   };
   switch (entry) {
     case MOE_ENTRY_ROUTE:
@@ -256,28 +258,27 @@ float router_gamma(const moe_config* c, const RouterPlan& rp) {
   return std::nextafter(static_cast<float>(g), INFINITY);
 }
 
-// Same for the warp-parallel fp64 re-decision: its own sum passes each product
-// through at most D/32 + 5 fp64 roundings, and the index-order definition
-// through D; the sum of both factors bounds |parallel - definition| / sum|x w|.
-double router_gamma64(const moe_config* c) {
-  const double u = std::ldexp(1.0, -53);
-  const double h1 = c->D / 32.0 + 6.0, h2 = c->D + 1.0;
-  return (h1 * u / (1.0 - h1 * u) + h2 * u / (1.0 - h2 * u)) * (1.0 + 1e-6) * 1.0001;
+// Level-2 radius factor (router.cu, warp_dot_comp): the compensated sum's
+// error-term chain has at most D/32 + 12 roundings over error terms totalling at
+// most (D/32 + 33) u sum|x w|; add the fp64 index-order definition's own
+// distance from the exact sum, (D + 2) 2^-53 sum|x w|.
+double router_gamma2(const moe_config* c) {
+  const double u = std::ldexp(1.0, -24);
+  const double n1 = c->D / 32.0 + 12.0, n2 = c->D / 32.0 + 33.0;
+  return (n1 * u / (1.0 - n1 * u)) * n2 * u * 1.01 + (c->D + 2.0) * std::ldexp(1.0, -53) * 1.01;
 }
 
 int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* wr,
                const float* bias, int32_t* blob, void* ws, const Layout& L, cudaStream_t st) {
   const RouterPlan rp = router_plan(c);
-  // Clears the status word and the refine counter for this call.
-  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // Clears the status word and the two refinement counters for this call.
+  if (cudaMemsetAsync(ws, 0, 12, st) != cudaSuccess) return MOE_ERR_CUDA;
   float* zpart = at<float>(ws, L.zpart);
-  float* xn = at<float>(ws, L.xnorm);
-  float* wn = at<float>(ws, L.wnorm);
-  launch_row_norms(x, c->T, c->D, xn, st);
-  launch_row_norms(wr, c->E, c->D, wn, st);
-  launch_router_logits(x, wr, c->T, c->D, c->E, rp.S, rp.sub_per_split, zpart, st);
-  return cuda_rc(launch_router_select(zpart, rp.S, c->T, c->D, c->E, c->k, bias, xn, wn,
-                                      router_gamma(c, rp), router_gamma64(c), x, wr, blob,
+  float* xsq = at<float>(ws, L.xnorm);
+  float* wsq = at<float>(ws, L.wnorm);
+  launch_router_logits(x, wr, c->T, c->D, c->E, rp.S, rp.sub_per_split, zpart, xsq, wsq, st);
+  return cuda_rc(launch_router_select(zpart, rp.S, c->T, c->D, c->E, c->k, bias, xsq, wsq,
+                                      router_gamma(c, rp), router_gamma2(c), x, wr, blob,
                                       at<int>(ws, 4), st));
 }
 

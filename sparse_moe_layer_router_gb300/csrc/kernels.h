@@ -10,13 +10,13 @@ namespace moe {
 constexpr int kPermuteChunk = 2048;  // pairs per permute block
 
 // ---- router (router.cu)
-void launch_row_norms(const void* a, int rows, int cols, float* out, cudaStream_t st);
 void launch_router_logits(const void* x, const void* wr, int T, int D, int E, int S,
-                          int sub_per_split, float* z_part, cudaStream_t st);
+                          int sub_per_split, float* z_part, float* xsq_part, float* wsq_part,
+                          cudaStream_t st);
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
-                                 const float* bias, const float* xnorm, const float* wnorm,
-                                 float gamma, double gamma64, const void* x, const void* wr,
-                                 int32_t* blob, int* refine_count, cudaStream_t st);
+                                 const float* bias, const float* xsq_part, const float* wsq_part,
+                                 float gamma, double gamma2, const void* x, const void* wr,
+                                 int32_t* blob, int* counters, cudaStream_t st);
 
 // ---- dispatch (permute.cu)
 cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,

@@ -14,110 +14,104 @@
 // Cauchy-Schwarz bound on sum |x_d Wr_ed|, plus the fp64 definition's own
 // deviation folded into gamma).  A token whose k-th / (k+1)-th boundary is
 // separated by these intervals is certified; otherwise the experts whose
-// intervals straddle the boundary are recomputed with the defining fp64
-// index-order sum and the boundary is re-decided exactly (ties: lower index).
+// intervals straddle the boundary are recomputed with a compensated fp32 dot
+// product whose rigorous radius is ~1e-10 of sum |x_d w_d| (level 2), and only
+// if that still cannot separate them with the defining fp64 index-order sum
+// itself (level 3: exact ties).  The result equals the definition's decision
+// (ties: lower index).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
-// ---------------------------------------------------------------- norms
-// out[row] >= || a[row, :] ||_2 (rigorous upper bound; see the margin below).
-__global__ void __launch_bounds__(256) row_norm_bound_kernel(const __nv_bfloat16* __restrict__ a,
-                                                             int rows, int cols,
-                                                             float* __restrict__ out) {
-  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint4* p = reinterpret_cast<const uint4*>(a + static_cast<size_t>(row) * cols);
-  float s = 0.f;
-  for (int i = lane; i < cols / 8; i += 32) {
-    const uint4 v = __ldg(p + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __uint_as_float(w[j] << 16);
-      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
-      s = fmaf(lo, lo, s);
-      s = fmaf(hi, hi, s);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) {
-    // Sum of non-negative terms with chain length <= cols/32*... + 5: relative
-    // error below 2^-10 for cols <= 2^16; sqrt and products add 2^-20 slack.
-    out[row] = sqrtf(s * (1.0f + 0x1p-10f)) * (1.0f + 0x1p-20f);
-  }
-}
-
 // ---------------------------------------------------------------- logits
 // z_part[split][t][e] = sum over the split's K range of x[t,k] * Wr[e,k] (fp32).
 // Within the range, products are accumulated in sub-chunks of 64 (a fresh fp32
-// accumulator each), and sub-chunk sums are added to the running total: each
+// accumulator each) and sub-chunk sums are added to the running total, so each
 // product passes through at most 64 + sub_per_split roundings.
+// The same pass also produces partial sums of squares of the x rows (CTAs with
+// blockIdx.x == 0) and of the router rows (blockIdx.y == 0) for the error
+// radius; every element is squared once per split.
+// Global loads of chunk c+1 are issued before chunk c is multiplied (register
+// staging, two shared-memory buffers, one barrier per 32-wide chunk).
 constexpr int kRT = 64, kRE = 64, kRK = 32;
 
 __global__ void __launch_bounds__(256) router_logits_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wr, int T, int D,
-    int E, int sub_per_split, float* __restrict__ z_part) {
-  __shared__ __align__(16) float xs[kRK][kRT + 4];
-  __shared__ __align__(16) float ws[kRK][kRE + 4];
+    int E, int sub_per_split, float* __restrict__ z_part, float* __restrict__ xsq_part,
+    float* __restrict__ wsq_part) {
+  __shared__ __align__(16) float xs[2][kRK][kRT + 4];
+  __shared__ __align__(16) float ws[2][kRK][kRE + 4];
   const int e0 = blockIdx.x * kRE, t0 = blockIdx.y * kRT, split = blockIdx.z;
   const int nsub = D / 64;
   const int sub_begin = split * sub_per_split;
   const int sub_end = min(nsub, sub_begin + sub_per_split);
+  const int nchunks = 2 * max(0, sub_end - sub_begin);
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int lrow = tid >> 2, lk = (tid & 3) * 8;
-  float acc[4][4];
+  const bool xrow_ok = t0 + lrow < T, wrow_ok = e0 + lrow < E;
+  const __nv_bfloat16* xsrc = x + static_cast<size_t>(t0 + lrow) * D + lk;
+  const __nv_bfloat16* wsrc = wr + static_cast<size_t>(e0 + lrow) * D + lk;
+  uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
+  float xsq = 0.f, wsq = 0.f;
+
+  auto gload = [&](int c) {
+    const int kbase = sub_begin * 64 + c * kRK;
+    if (xrow_ok) xv = __ldg(reinterpret_cast<const uint4*>(xsrc + kbase));
+    if (wrow_ok) wv = __ldg(reinterpret_cast<const uint4*>(wsrc + kbase));
+  };
+  auto sstore = [&](int buf) {
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float xl = __uint_as_float(xw[j] << 16), xh = __uint_as_float(xw[j] & 0xFFFF0000u);
+      const float wl = __uint_as_float(ww[j] << 16), wh = __uint_as_float(ww[j] & 0xFFFF0000u);
+      xs[buf][lk + 2 * j][lrow] = xl;
+      xs[buf][lk + 2 * j + 1][lrow] = xh;
+      ws[buf][lk + 2 * j][lrow] = wl;
+      ws[buf][lk + 2 * j + 1][lrow] = wh;
+      xsq = fmaf(xh, xh, fmaf(xl, xl, xsq));
+      wsq = fmaf(wh, wh, fmaf(wl, wl, wsq));
+    }
+  };
+
+  float acc[4][4], part[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc[i][j] = part[i][j] = 0.f;
 
-  for (int sub = sub_begin; sub < sub_end; ++sub) {
-    float part[4][4];
+  if (nchunks > 0) {
+    gload(0);
+    sstore(0);
+  }
+  __syncthreads();
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
+    if (c + 1 < nchunks) gload(c + 1);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int kk = 0; kk < kRK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      const int kbase = sub * 64 + half * 32;
-      uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
-      if (t0 + lrow < T)
-        xv = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + lrow) * D + kbase +
-                                                  lk));
-      if (e0 + lrow < E)
-        wv = __ldg(reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e0 + lrow) * D +
-                                                  kbase + lk));
-      __syncthreads();
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xs[lk + 2 * j][lrow] = __uint_as_float(xw[j] << 16);
-        xs[lk + 2 * j + 1][lrow] = __uint_as_float(xw[j] & 0xFFFF0000u);
-        ws[lk + 2 * j][lrow] = __uint_as_float(ww[j] << 16);
-        ws[lk + 2 * j + 1][lrow] = __uint_as_float(ww[j] & 0xFFFF0000u);
-      }
-      __syncthreads();
-#pragma unroll
-      for (int kk = 0; kk < kRK; ++kk) {
-        const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
-        const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-        const float av[4] = {a.x, a.y, a.z, a.w};
-        const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
-      }
+        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
     }
+    if (c & 1) {  // end of a 64-wide sub-chunk
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] += part[i][j];
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] += part[i][j];
+          part[i][j] = 0.f;
+        }
+    }
+    if (c + 1 < nchunks) sstore(buf ^ 1);
+    __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -130,17 +124,42 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
       if (e < E) dst[e] = acc[i][j];
     }
   }
+  // four threads share each staged row: combine their squares
+  xsq += __shfl_xor_sync(0xffffffffu, xsq, 1);
+  xsq += __shfl_xor_sync(0xffffffffu, xsq, 2);
+  wsq += __shfl_xor_sync(0xffffffffu, wsq, 1);
+  wsq += __shfl_xor_sync(0xffffffffu, wsq, 2);
+  if ((tid & 3) == 0) {
+    if (blockIdx.x == 0 && xrow_ok) xsq_part[static_cast<size_t>(split) * T + t0 + lrow] = xsq;
+    if (blockIdx.y == 0 && wrow_ok) wsq_part[static_cast<size_t>(split) * E + e0 + lrow] = wsq;
+  }
 }
 
 // ---------------------------------------------------------------- select
-// Warp-cooperative fp64 dot product of a token row and a router row: lane l
-// sums the 8-element groups l, l+32, ... in order (products are exact in
-// fp64), then a 5-level butterfly.  Each product passes through at most
-// D/32 + 5 fp64 roundings.  Every lane returns the same value (+ bias).
-__device__ double warp_dot_f64(const __nv_bfloat16* __restrict__ xr,
+// Upper bound of a Euclidean norm from split partial sums of squares: the fp32
+// sums pass each square through at most D/4 + S + 2 roundings (relative error
+// below 2^-9 for D <= 65536); sqrt and the products add 2^-20 of slack.
+__device__ __forceinline__ float norm_bound(float sumsq) {
+  return sqrtf(sumsq * (1.0f + 0x1p-9f)) * (1.0f + 0x1p-20f);
+}
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);  // a + b == s + e exactly
+}
+
+// Level 2: compensated fp32 dot product of a token row and a router row (+ bias),
+// warp-cooperative.  Products of two bf16 are exact in fp32; every addition is
+// an error-free TwoSum whose error term is collected in `c`; lanes combine
+// (sum, error) pairs with TwoSum in a butterfly, so every lane ends with the
+// same value.  |result - exact| <= 2^-52 |result| + gamma2 * sum|x_d w_d|, with
+// gamma2 set by the host from D (about 1e-10 at D = 4096).  The (sum, error)
+// pair is returned unrounded as s + c in fp64 (exact but for 2^-53 |result|).
+__device__ double warp_dot_comp(const __nv_bfloat16* __restrict__ xr,
                                const __nv_bfloat16* __restrict__ wrow, int D,
                                const float* __restrict__ bias, int e, int lane) {
-  double acc = 0.0;
+  float s = 0.f, c = 0.f;
   const uint4* xp = reinterpret_cast<const uint4*>(xr);
   const uint4* wp = reinterpret_cast<const uint4*>(wrow);
 #pragma unroll 4
@@ -150,21 +169,37 @@ __device__ double warp_dot_f64(const __nv_bfloat16* __restrict__ xr,
     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      acc = fma(static_cast<double>(__uint_as_float(xw[j] << 16)),
-                static_cast<double>(__uint_as_float(ww[j] << 16)), acc);
-      acc = fma(static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u)),
-                static_cast<double>(__uint_as_float(ww[j] & 0xFFFF0000u)), acc);
+      float t, err;
+      two_sum(s, __uint_as_float(xw[j] << 16) * __uint_as_float(ww[j] << 16), t, err);
+      s = t;
+      c += err;
+      two_sum(s, __uint_as_float(xw[j] & 0xFFFF0000u) * __uint_as_float(ww[j] & 0xFFFF0000u), t,
+              err);
+      s = t;
+      c += err;
     }
   }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (bias) acc += static_cast<double>(bias[e]);
-  return acc;
+  for (int o = 16; o; o >>= 1) {
+    const float so = __shfl_xor_sync(0xffffffffu, s, o);
+    const float co = __shfl_xor_sync(0xffffffffu, c, o);
+    float t, err;
+    two_sum(s, so, t, err);
+    s = t;
+    c = (c + co) + err;
+  }
+  if (bias) {
+    float t, err;
+    two_sum(s, bias[e], t, err);
+    s = t;
+    c += err;
+  }
+  return static_cast<double>(s) + static_cast<double>(c);
 }
 
-// The defining logit itself: fp64 sum in index order d = 0..D-1 of the exact
-// products (+ bias last).  The warp stages 256-element chunks of both rows in
-// shared memory (`stage`: 2 x 256 bf16 per warp); lane 0 runs the chain.
+// Level 3: the defining logit itself -- fp64 sum in index order d = 0..D-1 of
+// the exact products (+ bias last).  The warp stages 256-element chunks of both
+// rows in shared memory (`stage`: 2 x 256 bf16 per warp); lane 0 runs the chain.
 // Every lane returns the value.
 __device__ double warp_exact_logit(const __nv_bfloat16* __restrict__ xr,
                                    const __nv_bfloat16* __restrict__ wrow, int D,
@@ -189,10 +224,12 @@ __device__ double warp_exact_logit(const __nv_bfloat16* __restrict__ xr,
         const uint32_t ww[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          acc = fma(static_cast<double>(__uint_as_float(xw[j] << 16)),
-                    static_cast<double>(__uint_as_float(ww[j] << 16)), acc);
-          acc = fma(static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u)),
-                    static_cast<double>(__uint_as_float(ww[j] & 0xFFFF0000u)), acc);
+          // the fp32 product of two bf16 is exact, so adding it in fp64 is the
+          // definition's step
+          acc += static_cast<double>(__uint_as_float(xw[j] << 16) *
+                                     __uint_as_float(ww[j] << 16));
+          acc += static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u) *
+                                     __uint_as_float(ww[j] & 0xFFFF0000u));
         }
       }
     }
@@ -212,10 +249,10 @@ __device__ __forceinline__ bool better_d(double v, int e, double bv, int be) {
 template <int VPL>
 __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ z_part, int S, int T, int D, int E, int k,
-    const float* __restrict__ bias, const float* __restrict__ xnorm,
-    const float* __restrict__ wnorm, float gamma, const __nv_bfloat16* __restrict__ x,
+    const float* __restrict__ bias, const float* __restrict__ xsq_part,
+    const float* __restrict__ wsq_part, float gamma, const __nv_bfloat16* __restrict__ x,
     const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
-    int* __restrict__ refine_count, double gamma64) {
+    int* __restrict__ counters, double gamma2) {
   extern __shared__ double zx_smem[];  // [8 warps][E] refined logits, then [8][64] uint4 staging
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + wib;
@@ -223,30 +260,38 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   double* zx = zx_smem + static_cast<size_t>(wib) * E;
   uint4* stage = reinterpret_cast<uint4*>(zx_smem + static_cast<size_t>(8) * E) + wib * 64;
 
-  float v[VPL], r[VPL];
+  float v[VPL], r[VPL], wn[VPL];
   uint32_t sel = 0, cand = 0;
-  const float xn = xnorm[t];
-  // Split-K partials summed in split order; the VPL loads of one split are
-  // independent (and coalesced across the warp), so they are issued together.
+  // Split-K partials (logits and sums of squares) summed in split order; the
+  // VPL loads of one split are independent and coalesced across the warp.
+  float xsq = 0.f;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) v[i] = 0.f;
+  for (int i = 0; i < VPL; ++i) v[i] = wn[i] = 0.f;
   for (int sp = 0; sp < S; ++sp) {
     const float* zp = z_part + (static_cast<size_t>(sp) * T + t) * E;
-    float part[VPL];
+    const float* wp = wsq_part + static_cast<size_t>(sp) * E;
+    float part[VPL], sq[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
       part[i] = e < E ? __ldg(zp + e) : 0.f;
+      sq[i] = e < E ? __ldg(wp + e) : 0.f;
     }
+    xsq += __ldg(xsq_part + static_cast<size_t>(sp) * T + t);
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) v[i] += part[i];
+    for (int i = 0; i < VPL; ++i) {
+      v[i] += part[i];
+      wn[i] += sq[i];
+    }
   }
+  const float xn = norm_bound(xsq);
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
+    wn[i] = norm_bound(wn[i]);
     if (e < E) {
       if (bias) v[i] += __ldg(bias + e);
-      r[i] = gamma * xn * __ldg(wnorm + e) * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]);
+      r[i] = gamma * xn * wn[i] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]);
     } else {
       v[i] = -INFINITY;
       r[i] = 0.f;
@@ -309,9 +354,9 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     int slots = __popc(sel & cand);
 #pragma unroll
     for (int o = 16; o; o >>= 1) slots += __shfl_xor_sync(0xffffffffu, slots, o);
-    if (lane == 0 && refine_count) atomicAdd(refine_count, 1);
+    if (lane == 0 && counters) atomicAdd(counters, 1);
     const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
-    // Level 2: warp-parallel fp64 logits of every candidate.
+    // Level 2: compensated fp32 logits of every candidate.
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
@@ -319,7 +364,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
         const int src = __ffs(bal) - 1;
         bal &= bal - 1;
         const int e = src + 32 * i;
-        const double z = warp_dot_f64(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
+        const double z = warp_dot_comp(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
         if (lane == src) zx[e] = z;
       }
     }
@@ -351,15 +396,17 @@ __global__ void __launch_bounds__(256) router_select_kernel(
       }
     };
     pick(slots);
-    // Certified at fp64 level?  Radius: (parallel-sum + index-order-sum error
-    // factor) * ||x|| * ||w_e|| + 2^-52 |z| for the bias addition.
+    // Certified at level 2?  Radius: 2^-51 |z| (the fp64 pair sum, with slack)
+    // + gamma2 * (||x|| ||w_e|| + |bias_e|), gamma2 also covering the fp64
+    // index-order definition's own distance from the exact sum.
     double lo = INFINITY, hi = -INFINITY;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
       if (!((cand >> i) & 1u)) continue;
-      const double R = gamma64 * static_cast<double>(xn) * static_cast<double>(wnorm[e]) +
-                       0x1p-52 * fabs(zx[e]);
+      const double a = static_cast<double>(xn) * static_cast<double>(wn[i]) +
+                       (bias ? fabs(static_cast<double>(bias[e])) : 0.0);
+      const double R = gamma2 * a + 0x1p-51 * fabs(zx[e]);
       if ((chosen >> i) & 1u)
         lo = fmin(lo, zx[e] - R);
       else
@@ -372,6 +419,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     }
     if (!(lo > hi)) {
       // Level 3: the defining index-order fp64 sum (exact ties end here).
+      if (lane == 0 && counters) atomicAdd(counters + 1, 1);
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
@@ -431,25 +479,19 @@ __global__ void __launch_bounds__(256) router_select_kernel(
 }
 
 // ---------------------------------------------------------------- launchers
-void launch_row_norms(const void* a, int rows, int cols, float* out, cudaStream_t st) {
-  const int warps_per_block = 8;
-  const int blocks = (rows + warps_per_block - 1) / warps_per_block;
-  row_norm_bound_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a), rows, cols,
-                                                out);
-}
-
 void launch_router_logits(const void* x, const void* wr, int T, int D, int E, int S,
-                          int sub_per_split, float* z_part, cudaStream_t st) {
+                          int sub_per_split, float* z_part, float* xsq_part, float* wsq_part,
+                          cudaStream_t st) {
   dim3 grid((E + kRE - 1) / kRE, (T + kRT - 1) / kRT, S);
   router_logits_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
                                              static_cast<const __nv_bfloat16*>(wr), T, D, E,
-                                             sub_per_split, z_part);
+                                             sub_per_split, z_part, xsq_part, wsq_part);
 }
 
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
-                                 const float* bias, const float* xnorm, const float* wnorm,
-                                 float gamma, double gamma64, const void* x, const void* wr,
-                                 int32_t* blob, int* refine_count, cudaStream_t st) {
+                                 const float* bias, const float* xsq_part, const float* wsq_part,
+                                 float gamma, double gamma2, const void* x, const void* wr,
+                                 int32_t* blob, int* counters, cudaStream_t st) {
   const int blocks = (T + 7) / 8;
   const size_t smem = static_cast<size_t>(8) * E * sizeof(double) + 8 * 64 * sizeof(uint4);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
@@ -462,9 +504,9 @@ cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E
                                             static_cast<int>(smem));                         \
       if (e_ != cudaSuccess) return e_;                                                      \
     }                                                                                        \
-    router_select_kernel<V><<<blocks, 256, smem, st>>>(z_part, S, T, D, E, k, bias, xnorm,   \
-                                                       wnorm, gamma, xb, wb, blob,           \
-                                                       refine_count, gamma64);               \
+    router_select_kernel<V><<<blocks, 256, smem, st>>>(z_part, S, T, D, E, k, bias, xsq_part, \
+                                                       wsq_part, gamma, xb, wb, blob,        \
+                                                       counters, gamma2);                    \
     return cudaGetLastError();                                                               \
   }
   MOE_SELECT_CASE(1)
