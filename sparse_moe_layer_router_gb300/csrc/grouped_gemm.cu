@@ -39,21 +39,40 @@ constexpr int kAStage = kBM * kBK * 2;      // 16 KB bf16 operand tile
 constexpr int kARawStage = kBM * kBK / 2;   // 4 KB packed int4 tile
 constexpr int kMaxGroups = 1025;
 constexpr int kDequantWarps = 8;
+constexpr int kDequantGroups = 4;  // groups restore different pipeline stages concurrently
+constexpr int kWarpsPerGroup = kDequantWarps / kDequantGroups;
 
 template <int QUANT>
 struct GemmRoles {
   static constexpr int kThreads = QUANT ? 192 + 32 * kDequantWarps : 192;
-  static constexpr int kEmptyArrivals = QUANT ? 1 + kDequantWarps : 1;
+  // a stage is released by the MMA commit and, for W4A16, by the warps of the
+  // one dequant group that restored it
+  static constexpr int kEmptyArrivals = QUANT ? 1 + kWarpsPerGroup : 1;
 };
+
+// W4A16: the raw ring (packed int4 + token tile, STAGES deep, filled by TMA) is
+// decoupled from a shallow ring of kABufs restored bf16 operand tiles.
+constexpr int kABufs = 4;
+static_assert(kABufs % kDequantGroups == 0, "each operand buffer belongs to one group");
+
+// W4A16 group scales of one tile (128 rows x up to 32 groups), double buffered
+// across tiles and filled by TMA (used when K is a multiple of 1024 and <= 4096).
+constexpr int kScaleTabElems = kBM * 32;
 
 template <int BN_MAX, int STAGES, int QUANT>
 struct GemmSmem {
-  uint8_t a[STAGES][kAStage];                             // bf16 operand, 128-B swizzle
-  uint8_t b[STAGES][BN_MAX * 128];                        // token rows, 128-B swizzle
+  static constexpr int kA = QUANT ? kABufs : STAGES;
+  static constexpr bool kScaleTab = QUANT && BN_MAX == 64;
+  uint8_t a[kA][kAStage];                                  // bf16 operand, 128-B swizzle
+  uint8_t b[STAGES][BN_MAX * 128];                         // token rows, 128-B swizzle
   uint8_t araw[QUANT ? STAGES : 1][QUANT ? kARawStage : 16];  // packed int4 rows (W4A16)
+  uint16_t stab[kScaleTab ? 2 : 1][kScaleTab ? kScaleTabElems : 8];  // W4A16 tile scales
+  uint64_t sfull[2];
+  uint64_t sempty[2];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t aready[STAGES];
+  uint64_t aready[kA];
+  uint64_t afree[kA];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -169,7 +188,9 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_a_s,
                         const __grid_constant__ CUtensorMap tm_b,
-                        const __grid_constant__ CUtensorMap tm_b_s, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tm_b_s,
+                        const __grid_constant__ CUtensorMap tm_sc,
+                        const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = GemmSmem<BN_MAX, STAGES, QUANT>;
   constexpr int kThreads = GemmRoles<QUANT>::kThreads;
@@ -185,7 +206,14 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], GemmRoles<QUANT>::kEmptyArrivals);
-      mbar_init(&s.aready[i], kDequantWarps);
+    }
+    for (int i = 0; i < Smem::kA; ++i) {
+      mbar_init(&s.aready[i], kWarpsPerGroup);
+      mbar_init(&s.afree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.sfull[i], 1);
+      mbar_init(&s.sempty[i], kDequantWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -251,6 +279,8 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;  // bit i: stage i had a load issued; its phase in issued_ph
       uint32_t issued_ph = 0;
+      uint32_t tile_ctr = 0;  // W4A16 scale tables issued
+      uint32_t sissued = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
         const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
@@ -258,6 +288,27 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
         const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
         const uint32_t bytes = kABytes + static_cast<uint32_t>(t.bn) * 128u;
         const int a_row0 = t.shared ? 0 : t.e * p.a_rows_per_expert;
+        if (Smem::kScaleTab && p.scale_table) {
+          // this tile's group scales: 128 rows x K/128 groups, same row order as the weights
+          const int sb = tile_ctr & 1;
+          if (!mbar_wait(&s.sempty[sb], ((tile_ctr >> 1) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int ngrp = (t.shared ? p.K_s : p.K) / p.group;
+          const CUtensorMap* msc = t.shared ? &tm_sc_s : &tm_sc;
+          mbar_arrive_expect_tx(&s.sfull[sb], static_cast<uint32_t>(kBM * ngrp * 2));
+          if (p.op == kOpGateUp) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              tma_load_3d(s.stab[sb] + b * 32 * ngrp, msc, &s.sfull[sb], 0,
+                          a_row0 + t.m * 64 + 16 * b, 0, pol_w);
+          } else {
+            tma_load_2d(s.stab[sb], msc, &s.sfull[sb], 0, a_row0 + t.m * kBM, pol_w);
+          }
+          sissued = 1u << sb;
+          ++tile_ctr;
+        }
         for (int kb = 0; kb < t.k_blocks; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -292,6 +343,10 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
         record_error(p, abort_flag, MOE_ERR_TIMEOUT);
         for (int i = 0; i < STAGES; ++i)
           if ((issued >> i) & 1u) mbar_wait_time_only(&s.full[i], (issued_ph >> i) & 1u);
+        if (sissued) {
+          const uint32_t last = tile_ctr - 1;
+          mbar_wait_time_only(&s.sfull[last & 1], (last >> 1) & 1u);
+        }
       }
     }
   } else if (warp == 1) {
@@ -299,6 +354,8 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
       // ------------------------------------------------ MMA issuer
       int stage = 0;
       uint32_t phase = 0;
+      int abuf = 0;  // W4A16: restored operand buffer and its phase
+      uint32_t aphase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -312,18 +369,25 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN_MAX);
         const uint32_t idesc = idesc_bf16_f32(kBM, t.bn);
         for (int kb = 0; kb < t.k_blocks; ++kb) {
-          if ((QUANT && !mbar_wait(&s.aready[stage], phase, abort_flag)) ||
+          if ((QUANT && !mbar_wait(&s.aready[abuf], aphase, abort_flag)) ||
               !mbar_wait(&s.full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_sw128(smem_u32(s.a[stage]));
+          const uint64_t ad = sdesc_sw128(smem_u32(s.a[QUANT ? abuf : stage]));
           const uint64_t bd = sdesc_sw128(smem_u32(s.b[stage]));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           mma_commit(&s.empty[stage]);
+          if (QUANT) {
+            mma_commit(&s.afree[abuf]);
+            if (++abuf == Smem::kA) {
+              abuf = 0;
+              aphase ^= 1u;
+            }
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -419,46 +483,81 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
     }
   } else if (QUANT) {
     // -------------------------------------------------- dequant (warps 6-13, W4A16)
-    // Thread -> (tile row r, half of its 8 packed words).  Reads 16 B of packed
-    // int4, writes four 16-B chunks of bf16 into the 128-B-swizzled operand
-    // tile: chunk c of row r lives at r*128 + ((c ^ (r & 7)) << 4).
-    const int td = (warp - 6) * 32 + lane;
-    const int r = td >> 1, half = td & 1;
-    int stage = 0;
-    uint32_t phase = 0;
+    // kDequantGroups groups of kWarpsPerGroup warps.  The running k-block index
+    // i goes to group i mod kDequantGroups; since the raw ring depth and the
+    // operand ring depth are both multiples of the group count, every raw stage
+    // and every operand buffer always belongs to the same group, so each group
+    // waits on each of its barriers in phase order.  Within a group, thread tg
+    // owns tile rows tg + 64 j: it reads the row's 32 B of packed int4 and writes
+    // eight 16-B chunks of bf16 into the 128-B-swizzled operand tile (chunk c of
+    // row r lives at r*128 + ((c ^ (r & 7)) << 4)).
+    constexpr int kGroupThreads = 32 * kWarpsPerGroup;
+    constexpr int kRowsPerThread = kBM / kGroupThreads;
+    static_assert(STAGES % kDequantGroups == 0, "raw stages must map to fixed groups");
+    const int dw = warp - 6;
+    const int grp = dw / kWarpsPerGroup;
+    const int tg = (dw % kWarpsPerGroup) * 32 + lane;
+    uint32_t idx = 0;  // running k-block index (the same sequence every role walks)
+    uint32_t tile_ctr = 0;
+    const bool table = Smem::kScaleTab && p.scale_table;
     bool ok = true;
     for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
       const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
       const int K = t.shared ? p.K_s : p.K;
-      const uint16_t* srow = (t.shared ? p.wscale_s : p.wscale) +
-                             static_cast<size_t>(tile_weight_row(p, t, r)) * (K / p.group);
-      for (int kb = 0; kb < t.k_blocks; ++kb) {
-        const uint16_t sbits = __ldg(srow + (kb * kBK) / p.group);
-        __nv_bfloat162 s2;
-        s2.x = __ushort_as_bfloat16(sbits);
-        s2.y = s2.x;
-        if (!mbar_wait(&s.full[stage], phase, abort_flag)) {
+      const int ngrp = K / p.group;
+      const uint16_t* sbase = t.shared ? p.wscale_s : p.wscale;
+      const uint16_t* srow[kRowsPerThread];
+#pragma unroll
+      for (int j = 0; j < kRowsPerThread; ++j)
+        srow[j] = sbase + static_cast<size_t>(tile_weight_row(p, t, tg + j * kGroupThreads)) * ngrp;
+      const int sb = tile_ctr & 1;
+      if (table && !mbar_wait(&s.sfull[sb], (tile_ctr >> 1) & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      for (int kb = 0; kb < t.k_blocks; ++kb, ++idx) {
+        if (static_cast<int>(idx % kDequantGroups) != grp) continue;
+        const int stage = static_cast<int>(idx % STAGES);
+        const uint32_t phase = (idx / STAGES) & 1u;
+        const int abuf = static_cast<int>(idx % kABufs);
+        const uint32_t aphase = (idx / kABufs) & 1u;
+        __nv_bfloat162 s2[kRowsPerThread];
+#pragma unroll
+        for (int j = 0; j < kRowsPerThread; ++j) {
+          const int g = (kb * kBK) / p.group;
+          const uint16_t sbits = table ? s.stab[sb][(tg + j * kGroupThreads) * ngrp + g]
+                                       : __ldg(srow[j] + g);
+          s2[j].x = __ushort_as_bfloat16(sbits);
+          s2[j].y = s2[j].x;
+        }
+        if (!mbar_wait(&s.full[stage], phase, abort_flag) ||
+            !mbar_wait(&s.afree[abuf], aphase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        const uint4 pk = *reinterpret_cast<const uint4*>(s.araw[stage] + r * 32 + half * 16);
-        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
-        uint8_t* arow = s.a[stage] + r * 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = half * 4 + i;
-          *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(words[i], s2);
+        for (int j = 0; j < kRowsPerThread; ++j) {
+          const int r = tg + j * kGroupThreads;
+          const uint4 p0 = *reinterpret_cast<const uint4*>(s.araw[stage] + r * 32);
+          const uint4 p1 = *reinterpret_cast<const uint4*>(s.araw[stage] + r * 32 + 16);
+          const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          uint8_t* arow = s.a[abuf] + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(words[c], s2[j]);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&s.aready[stage]);
+          mbar_arrive(&s.aready[abuf]);
           mbar_arrive(&s.empty[stage]);
         }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      }
+      if (!ok) break;
+      if (table) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sempty[sb]);
+        ++tile_ctr;
       }
     }
     if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
@@ -480,7 +579,7 @@ static cudaError_t launch_variant(const GemmParams& p, const GemmMaps& m, int nu
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, GemmRoles<QUANT>::kThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, p);
+  kern<<<num_sms, GemmRoles<QUANT>::kThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
   return cudaGetLastError();
 }
 
@@ -490,7 +589,7 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int b
     if (bn_max == 64) return launch_variant<64, 8, 0>(p, maps, num_sms, st);
     if (bn_max == 256) return launch_variant<256, 4, 0>(p, maps, num_sms, st);
   } else if (quant == 1) {
-    if (bn_max == 64) return launch_variant<64, 7, 1>(p, maps, num_sms, st);
+    if (bn_max == 64) return launch_variant<64, 8, 1>(p, maps, num_sms, st);
     if (bn_max == 256) return launch_variant<256, 4, 1>(p, maps, num_sms, st);
   }
   return cudaErrorInvalidValue;

@@ -136,6 +136,31 @@ bool map_gate_up_i4(CUtensorMap* m, const void* base, uint64_t groups, uint64_t 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 group scales [rows][ngrp]: 2-D map with a {ngrp, box_rows} box (whole
+// rows of scales), or the 3-D gate/up pairing with a {ngrp, 16, 2} box.
+bool map_scales(CUtensorMap* m, const void* base, uint64_t groups, uint64_t rows_per_group,
+                uint64_t ngrp, bool gate_up) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  if (gate_up) {
+    const uint64_t half = rows_per_group / 2;
+    const cuuint64_t dims[3] = {ngrp, groups * rows_per_group, 2};
+    const cuuint64_t strides[2] = {ngrp * 2, half * ngrp * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(ngrp), 16, 2};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[2] = {ngrp, groups * rows_per_group};
+  const cuuint64_t strides[1] = {ngrp * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(ngrp), 128};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- validation
 int validate(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
@@ -262,10 +287,12 @@ float router_gamma(const moe_config* c, const RouterPlan& rp) {
 // error-term chain has at most D/32 + 12 roundings over error terms totalling at
 // most (D/32 + 33) u sum|x w|; add the fp64 index-order definition's own
 // distance from the exact sum, (D + 2) 2^-53 sum|x w|.
-double router_gamma2(const moe_config* c) {
+float router_gamma2(const moe_config* c) {
   const double u = std::ldexp(1.0, -24);
   const double n1 = c->D / 32.0 + 12.0, n2 = c->D / 32.0 + 33.0;
-  return (n1 * u / (1.0 - n1 * u)) * n2 * u * 1.01 + (c->D + 2.0) * std::ldexp(1.0, -53) * 1.01;
+  const double g = (n1 * u / (1.0 - n1 * u)) * n2 * u * 1.01 +
+                   (c->D + 2.0) * std::ldexp(1.0, -53) * 1.01;
+  return std::nextafter(static_cast<float>(g), INFINITY);
 }
 
 int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* wr,
@@ -351,12 +378,28 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, 16);
     }
   }
+  // W4A16 scale tables by TMA when every K of the launch is a multiple of 1024
+  // up to 4096 (whole rows of 8..32 scales, 16..64 B) and the 64-row variant runs.
+  const int bn_max = choose_bn_max(c);
+  const bool k_ok = p.K % 1024 == 0 && p.K <= 4096 && (!has_shared || (p.K_s % 1024 == 0 &&
+                                                                      p.K_s <= 4096));
+  p.scale_table = (w4 && bn_max == 64 && k_ok) ? 1 : 0;
+  if (p.scale_table) {
+    const uint64_t rows_r = gate_up ? 2ull * c->I : static_cast<uint64_t>(c->D);
+    ok &= map_scales(&maps.sc, a->w_scales, c->E, rows_r, p.K / c->group, gate_up);
+    if (has_shared) {
+      const uint64_t rows_s = gate_up ? 2ull * c->I_shared : static_cast<uint64_t>(c->D);
+      ok &= map_scales(&maps.sc_s, a->ws_scales, 1, rows_s, p.K_s / c->group, gate_up);
+    }
+  }
   if (!ok) return MOE_ERR_CUDA;
   if (!has_shared) {
     maps.a_s = maps.a;
     maps.b_s = maps.b;
   }
-  return cuda_rc(launch_grouped_gemm(p, maps, choose_bn_max(c), c->quant, dev.sms, st));
+  if (!p.scale_table || !has_shared) maps.sc_s = maps.a_s;
+  if (!p.scale_table) maps.sc = maps.a;
+  return cuda_rc(launch_grouped_gemm(p, maps, bn_max, c->quant, dev.sms, st));
 }
 
 int check_gemm_args(const moe_config* c, const moe_gemm_args* a) {

@@ -15,7 +15,7 @@ void launch_router_logits(const void* x, const void* wr, int T, int D, int E, in
                           cudaStream_t st);
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
                                  const float* bias, const float* xsq_part, const float* wsq_part,
-                                 float gamma, double gamma2, const void* x, const void* wr,
+                                 float gamma, float gamma2, const void* x, const void* wr,
                                  int32_t* blob, int* counters, cudaStream_t st);
 
 // ---- dispatch (permute.cu)
@@ -65,10 +65,12 @@ struct GemmParams {
   const uint16_t* wscale_s;
   int K, K_s;               // reduction sizes (elements)
   int group;
+  int scale_table;          // W4A16: tile scales come from tm_sc / tm_sc_s by TMA
 };
 
 struct GemmMaps {
   CUtensorMap a, a_s, b, b_s;  // weights (routed, shared), activations (routed, shared)
+  CUtensorMap sc, sc_s;        // W4A16 group scales (routed, shared)
 };
 
 // Kernel variants: BN_MAX token rows per tile (64 or 256); quant 0 = bf16, 1 = W4A16.

@@ -153,10 +153,10 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 // warp-cooperative.  Products of two bf16 are exact in fp32; every addition is
 // an error-free TwoSum whose error term is collected in `c`; lanes combine
 // (sum, error) pairs with TwoSum in a butterfly, so every lane ends with the
-// same value.  |result - exact| <= 2^-52 |result| + gamma2 * sum|x_d w_d|, with
+// same value.  |(s + c) - exact| <= gamma2 * sum|x_d w_d|, with
 // gamma2 set by the host from D (about 1e-10 at D = 4096).  The (sum, error)
-// pair is returned unrounded as s + c in fp64 (exact but for 2^-53 |result|).
-__device__ double warp_dot_comp(const __nv_bfloat16* __restrict__ xr,
+// pair (s, c) is returned unevaluated: the value is s + c.
+__device__ float2 warp_dot_comp(const __nv_bfloat16* __restrict__ xr,
                                const __nv_bfloat16* __restrict__ wrow, int D,
                                const float* __restrict__ bias, int e, int lane) {
   float s = 0.f, c = 0.f;
@@ -194,7 +194,7 @@ __device__ double warp_dot_comp(const __nv_bfloat16* __restrict__ xr,
     s = t;
     c += err;
   }
-  return static_cast<double>(s) + static_cast<double>(c);
+  return make_float2(s, c);
 }
 
 // Level 3: the defining logit itself -- fp64 sum in index order d = 0..D-1 of
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ bias, const float* __restrict__ xsq_part,
     const float* __restrict__ wsq_part, float gamma, const __nv_bfloat16* __restrict__ x,
     const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
-    int* __restrict__ counters, double gamma2) {
+    int* __restrict__ counters, float gamma2) {
   extern __shared__ double zx_smem[];  // [8 warps][E] refined logits, then [8][64] uint4 staging
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + wib;
@@ -356,23 +356,106 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     for (int o = 16; o; o >>= 1) slots += __shfl_xor_sync(0xffffffffu, slots, o);
     if (lane == 0 && counters) atomicAdd(counters, 1);
     const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
-    // Level 2: compensated fp32 logits of every candidate.
+    // Level 2: compensated fp32 logits of every candidate, kept as the
+    // unevaluated pair (s, c) by the lane that owns the expert.
+    float zs[VPL], zc[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
+      zs[i] = zc[i] = 0.f;
       uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
       while (bal) {
         const int src = __ffs(bal) - 1;
         bal &= bal - 1;
         const int e = src + 32 * i;
-        const double z = warp_dot_comp(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
-        if (lane == src) zx[e] = z;
+        const float2 sc = warp_dot_comp(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
+        if (lane == src) {
+          zs[i] = sc.x;
+          zc[i] = sc.y;
+        }
       }
     }
-    __syncwarp();
+    // Values relative to a common reference (the largest candidate sum s):
+    // rel = (s - ref) + c, with |rel - (z - ref)| <= 2^-23 |rel| (s - ref is
+    // exact when s is within a factor of two of ref), all in fp32.
+    float ref = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if ((cand >> i) & 1u) ref = fmaxf(ref, zs[i]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ref = fmaxf(ref, __shfl_xor_sync(0xffffffffu, ref, o));
+    float rel[VPL], rad[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      rel[i] = -INFINITY;
+      rad[i] = 0.f;
+      if ((cand >> i) & 1u) {
+        rel[i] = (zs[i] - ref) + zc[i];
+        const float a = xn * wn[i] + (bias ? fabsf(bias[e]) : 0.f);
+        // gamma2 * sum|x w| (level-2 error, plus the fp64 definition's own
+        // distance from the exact sum) + rounding of rel and of rel -/+ rad
+        rad[i] = gamma2 * a * (1.0f + 0x1p-20f) + 0x1p-21f * fabsf(rel[i]);
+      }
+    }
     uint32_t chosen = 0;
-    auto pick = [&](int nslots) {
+    for (int j = 0; j < slots; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (((cand >> i) & 1u) && !((chosen >> i) & 1u) && better(rel[i], e, bv, be)) {
+          bv = rel[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (better(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+    }
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (!((cand >> i) & 1u)) continue;
+      if ((chosen >> i) & 1u)
+        lo = fminf(lo, rel[i] - rad[i]);
+      else
+        hi = fmaxf(hi, rel[i] + rad[i]);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    // Refined logits replace the fp32 ones for the weights.
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if ((cand >> i) & 1u) v[i] = zs[i] + zc[i];
+    if (!(lo > hi)) {
+      // Level 3: the defining index-order fp64 sum (exact ties end here).
+      if (lane == 0 && counters) atomicAdd(counters + 1, 1);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
+        while (bal) {
+          const int src = __ffs(bal) - 1;
+          bal &= bal - 1;
+          const int e = src + 32 * i;
+          const double z =
+              warp_exact_logit(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane, stage);
+          if (lane == src) zx[e] = z;
+        }
+      }
+      __syncwarp();
       chosen = 0;
-      for (int j = 0; j < nslots; ++j) {
+      for (int j = 0; j < slots; ++j) {
         double bv = -INFINITY;
         int be = 0x7fffffff;
 #pragma unroll
@@ -394,54 +477,13 @@ __global__ void __launch_bounds__(256) router_select_kernel(
         }
         if ((be & 31) == lane) chosen |= 1u << (be >> 5);
       }
-    };
-    pick(slots);
-    // Certified at level 2?  Radius: 2^-51 |z| (the fp64 pair sum, with slack)
-    // + gamma2 * (||x|| ||w_e|| + |bias_e|), gamma2 also covering the fp64
-    // index-order definition's own distance from the exact sum.
-    double lo = INFINITY, hi = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (!((cand >> i) & 1u)) continue;
-      const double a = static_cast<double>(xn) * static_cast<double>(wn[i]) +
-                       (bias ? fabs(static_cast<double>(bias[e])) : 0.0);
-      const double R = gamma2 * a + 0x1p-51 * fabs(zx[e]);
-      if ((chosen >> i) & 1u)
-        lo = fmin(lo, zx[e] - R);
-      else
-        hi = fmax(hi, zx[e] + R);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      lo = fmin(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = fmax(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    if (!(lo > hi)) {
-      // Level 3: the defining index-order fp64 sum (exact ties end here).
-      if (lane == 0 && counters) atomicAdd(counters + 1, 1);
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
-        uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
-        while (bal) {
-          const int src = __ffs(bal) - 1;
-          bal &= bal - 1;
-          const int e = src + 32 * i;
-          const double z =
-              warp_exact_logit(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane, stage);
-          if (lane == src) zx[e] = z;
-        }
+        const int e = lane + 32 * i;
+        if ((cand >> i) & 1u) v[i] = static_cast<float>(zx[e]);
       }
-      __syncwarp();
-      pick(slots);
     }
     sel = (sel & ~cand) | chosen;
-    // Refined logits replace the fp32 ones for the weights.
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if ((cand >> i) & 1u) v[i] = static_cast<float>(zx[e]);
-    }
   }
 
   // Softmax over all E, renormalised over the selected k:
@@ -490,7 +532,7 @@ void launch_router_logits(const void* x, const void* wr, int T, int D, int E, in
 
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
                                  const float* bias, const float* xsq_part, const float* wsq_part,
-                                 float gamma, double gamma2, const void* x, const void* wr,
+                                 float gamma, float gamma2, const void* x, const void* wr,
                                  int32_t* blob, int* counters, cudaStream_t st) {
   const int blocks = (T + 7) / 8;
   const size_t smem = static_cast<size_t>(8) * E * sizeof(double) + 8 * 64 * sizeof(uint4);
