@@ -82,8 +82,9 @@ extern "C" {
  * Shapes of one layer call.
  *   T        tokens (1 .. 2^20), D hidden size (multiple of 128),
  *   E        routed experts (1 .. 1024), I / I_shared expert intermediate sizes
- *            (multiples of 64; of `group` for W4A16), k experts per token
- *            (1 .. min(E, 32)), quant MOE_QUANT_*, group = 128 for W4A16.
+ *            (multiples of 64), k experts per token (1 .. min(E, 32)),
+ *   quant    MOE_QUANT_*; for W4A16, group = 128 and D, I, I_shared are
+ *            multiples of 256 (packed K tiles of 256 values).
  */
 typedef struct moe_config {
   int T, D, E, I, I_shared, k;

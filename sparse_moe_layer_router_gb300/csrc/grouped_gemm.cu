@@ -13,9 +13,10 @@
 //     BN_MAX token rows x 64 K.  The MMA is "swap-AB": weights are the M = 128
 //     operand, tokens the N operand (16..BN_MAX, multiple of 16), so a group
 //     with few tokens still streams full-width weight tiles.
-//   * warp 0: TMA producer (one thread) into a STAGES-deep shared-memory ring;
-//     warp 1: TMEM allocation and tcgen05.mma issue (one thread), fp32
-//     accumulators in TMEM, double buffered; warps 2-5: epilogue (tcgen05.ld).
+//   * warp 0: TMA producer (one thread); warp 1: TMEM allocation and
+//     tcgen05.mma issue (one thread), fp32 accumulators in TMEM, double
+//     buffered; warps 2-5: epilogue (tcgen05.ld); W4A16 adds warps 6-13, which
+//     restore packed int4 tiles to the bf16 operand in shared memory.
 //   * Tiles: every CTA walks tile indices blockIdx.x, +gridDim.x, ... over the
 //     concatenation of groups [shared, expert 0, ..., expert E-1]; a group with
 //     R rows has ceil(R / BN_MAX) * m_tiles tiles, token tiles of one weight
@@ -35,44 +36,38 @@ namespace moe {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kAStage = kBM * kBK * 2;      // 16 KB bf16 operand tile
-constexpr int kARawStage = kBM * kBK / 2;   // 4 KB packed int4 tile
+constexpr int kAStage = kBM * kBK * 2;  // 16 KB bf16 operand tile
 constexpr int kMaxGroups = 1025;
-constexpr int kDequantWarps = 8;
-constexpr int kDequantGroups = 4;  // groups restore different pipeline stages concurrently
-constexpr int kWarpsPerGroup = kDequantWarps / kDequantGroups;
+constexpr int kBaseThreads = 192;       // producer, MMA, 4 epilogue warps
 
-template <int QUANT>
-struct GemmRoles {
-  static constexpr int kThreads = QUANT ? 192 + 32 * kDequantWarps : 192;
-  // a stage is released by the MMA commit and, for W4A16, by the warps of the
-  // one dequant group that restored it
-  static constexpr int kEmptyArrivals = QUANT ? 1 + kWarpsPerGroup : 1;
+// W4A16: packed stages of 128 rows x 128 B (256 int4 values = 4 k-blocks).
+// Two dequant groups of four warps (one tile row per thread); group g restores
+// k-blocks 4q + g and 4q + 2 + g of packed stage q into its two operand
+// buffers 2g and 2g + 1, so it restores one while the MMA reads the other.
+constexpr int kPackedK = 256;
+constexpr int kPackedStage = kBM * kPackedK / 2;  // 16 KB
+constexpr int kKPerPacked = kPackedK / kBK;       // 4 k-blocks per packed stage
+constexpr int kABuffers = 4;
+constexpr int kDequantGroups = 2;
+constexpr int kWarpsPerGroup = 4;
+constexpr int kDequantWarps = kDequantGroups * kWarpsPerGroup;
+constexpr int kTokenWarp = 6 + kDequantWarps;  // W4A16: separate producer for token tiles
+constexpr int kW4Threads = kBaseThreads + 32 * kDequantWarps + 32;
+constexpr int kScaleTabElems = kBM * 32;  // one tile's scales for K <= 4096
+
+struct TileInfo {
+  int shared;
+  int e;
+  int m;
+  int n_valid;
+  int bn;
+  int b_row;
+  int k_blocks;
 };
 
-// W4A16: the raw ring (packed int4 + token tile, STAGES deep, filled by TMA) is
-// decoupled from a shallow ring of kABufs restored bf16 operand tiles.
-constexpr int kABufs = 4;
-static_assert(kABufs % kDequantGroups == 0, "each operand buffer belongs to one group");
-
-// W4A16 group scales of one tile (128 rows x up to 32 groups), double buffered
-// across tiles and filled by TMA (used when K is a multiple of 1024 and <= 4096).
-constexpr int kScaleTabElems = kBM * 32;
-
-template <int BN_MAX, int STAGES, int QUANT>
-struct GemmSmem {
-  static constexpr int kA = QUANT ? kABufs : STAGES;
-  static constexpr bool kScaleTab = QUANT && BN_MAX == 64;
-  uint8_t a[kA][kAStage];                                  // bf16 operand, 128-B swizzle
-  uint8_t b[STAGES][BN_MAX * 128];                         // token rows, 128-B swizzle
-  uint8_t araw[QUANT ? STAGES : 1][QUANT ? kARawStage : 16];  // packed int4 rows (W4A16)
-  uint16_t stab[kScaleTab ? 2 : 1][kScaleTab ? kScaleTabElems : 8];  // W4A16 tile scales
-  uint64_t sfull[2];
-  uint64_t sempty[2];
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t aready[kA];
-  uint64_t afree[kA];
+// Shared-memory parts common to both kernels.
+template <int BN_MAX>
+struct GemmCommon {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -83,14 +78,26 @@ struct GemmSmem {
   float row_weight[4][BN_MAX];  // down epilogue: routing weight of each token row, per warp
 };
 
-struct TileInfo {
-  int shared;
-  int e;
-  int m;
-  int n_valid;
-  int bn;
-  int b_row;
-  int k_blocks;
+template <int BN_MAX, int STAGES>
+struct Bf16Smem {
+  uint8_t a[STAGES][kAStage];       // weights, 128-B swizzle
+  uint8_t b[STAGES][BN_MAX * 128];  // token rows, 128-B swizzle
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  GemmCommon<BN_MAX> c;
+};
+
+template <int BN_MAX, int PSTAGES, int BSTAGES>
+struct W4Smem {
+  uint8_t a[kABuffers][kAStage];        // restored bf16 operand, two per dequant group
+  uint8_t b[BSTAGES][BN_MAX * 128];     // token rows per k-block
+  uint8_t praw[PSTAGES][kPackedStage];  // packed int4 rows, 128-B swizzle
+  uint16_t stab[2][kScaleTabElems];     // group scales of the current tiles
+  uint64_t pfull[PSTAGES], pempty[PSTAGES];
+  uint64_t bfull[BSTAGES], bempty[BSTAGES];
+  uint64_t aready[kABuffers], afree[kABuffers];
+  uint64_t sfull[2], sempty[2];
+  GemmCommon<BN_MAX> c;
 };
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -118,8 +125,9 @@ __device__ __forceinline__ void record_error(const GemmParams& p, volatile int* 
   if (p.status) atomicCAS(p.status, 0, code);
 }
 
-template <typename Smem, int BN_MAX>
-__device__ __forceinline__ TileInfo decode_tile(const Smem& s, const GemmParams& p, int G, int L) {
+template <int BN_MAX>
+__device__ __forceinline__ TileInfo decode_tile(const GemmCommon<BN_MAX>& s, const GemmParams& p,
+                                                int G, int L) {
   int lo = 0, hi = G;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -144,7 +152,10 @@ __device__ __forceinline__ TileInfo decode_tile(const Smem& s, const GemmParams&
   return t;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// First weight row of a tile in its weight map (routed maps stack experts).
+__device__ __forceinline__ int tile_a_row(const GemmParams& p, const TileInfo& t) {
+  return (t.shared ? 0 : t.e * p.a_rows_per_expert) + t.m * (p.op == kOpGateUp ? 64 : kBM);
+}
 
 // Weight row (in the full weight matrix of its group) held by row r of a tile.
 // Gate/up tiles hold four blocks of (16 gate rows, 16 up rows) of features
@@ -159,6 +170,8 @@ __device__ __forceinline__ int tile_weight_row(const GemmParams& p, const TileIn
   }
   return (t.shared ? 0 : t.e * p.a_rows_per_expert) + t.m * kBM + r;
 }
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // Eight signed 4-bit values (value j in bits 4j..4j+3) times a bf16 scale ->
 // eight bf16 in order, each bf16_rne(q * s).  Nibbles become offset binary
@@ -183,58 +196,14 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   return out;
 }
 
-template <int BN_MAX, int STAGES, int QUANT>
-__global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                        const __grid_constant__ CUtensorMap tm_a_s,
-                        const __grid_constant__ CUtensorMap tm_b,
-                        const __grid_constant__ CUtensorMap tm_b_s,
-                        const __grid_constant__ CUtensorMap tm_sc,
-                        const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  using Smem = GemmSmem<BN_MAX, STAGES, QUANT>;
-  constexpr int kThreads = GemmRoles<QUANT>::kThreads;
-  const uint32_t raw = smem_u32(smem_raw);
-  Smem& s = *reinterpret_cast<Smem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
-  constexpr uint32_t kTmemCols = (2 * BN_MAX < 32) ? 32u : static_cast<uint32_t>(2 * BN_MAX);
-  constexpr uint32_t kABytes = QUANT ? kARawStage : kAStage;
-
+// Group table: s.off <- offsets, s.tile_start <- exclusive scan of tiles per
+// group; returns the number of tiles.  All threads of the CTA call it.
+template <int BN_MAX>
+__device__ int build_tile_table(GemmCommon<BN_MAX>& s, const GemmParams& p, int G, int nthreads) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = p.E + p.has_shared;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], GemmRoles<QUANT>::kEmptyArrivals);
-    }
-    for (int i = 0; i < Smem::kA; ++i) {
-      mbar_init(&s.aready[i], kWarpsPerGroup);
-      mbar_init(&s.afree[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.sfull[i], 1);
-      mbar_init(&s.sempty[i], kDequantWarps);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);
-    }
-    mbar_init(&s.drain, 1);
-    s.abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (threadIdx.x == 32) {
-    prefetch_tmap(&tm_a);
-    prefetch_tmap(&tm_b);
-    if (p.has_shared) {
-      prefetch_tmap(&tm_a_s);
-      prefetch_tmap(&tm_b_s);
-    }
-  }
-  for (int i = threadIdx.x; i <= p.E; i += kThreads) s.off[i] = p.offsets[i];
+  for (int i = threadIdx.x; i <= p.E; i += nthreads) s.off[i] = p.offsets[i];
   __syncthreads();
-  // Tiles per group, then an exclusive scan into tile_start.
-  for (int g = threadIdx.x; g < G; g += kThreads) {
+  for (int g = threadIdx.x; g < G; g += nthreads) {
     const bool sh = p.has_shared && g == 0;
     const int e = g - p.has_shared;
     const int rows = sh ? p.T_shared : s.off[e + 1] - s.off[e];
@@ -259,16 +228,155 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
     }
     if (lane == 0) s.tile_start[0] = 0;
   }
+  __syncthreads();
+  return s.tile_start[G];
+}
+
+template <int BN_MAX>
+__device__ __forceinline__ void init_common_barriers(GemmCommon<BN_MAX>& c) {
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&c.tfull[i], 1);
+    mbar_init(&c.tempty[i], 4);
+  }
+  mbar_init(&c.drain, 1);
+  c.abort_flag = 0;
+}
+
+// Epilogue role (warps 2-5): TMEM accumulators -> h (SwiGLU, bf16) or o
+// (routing-weighted, fp32).
+template <int BN_MAX>
+__device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G, int ntiles,
+                              uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
+  const int sp = warp & 3;  // TMEM lanes 32*sp .. 32*sp+31
+  float* wts = s.row_weight[warp - 2];
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int L = blockIdx.x; L < ntiles; L += gridDim.x) {
+    const TileInfo t = decode_tile<BN_MAX>(s, p, G, L);
+    if (p.op == kOpDown) {
+      // Routing weight of every token row of the tile, fetched before the
+      // accumulator is ready: row r holds pair p = perm_pair[r] (token p / k,
+      // slot p % k); the shared group has weight 1.
+      __syncwarp();
+      for (int j = lane; j < t.n_valid; j += 32) {
+        float wgt = 1.0f;
+        if (!t.shared) {
+          const int pr = __ldg(p.perm_pair + t.b_row + j);
+          const int tk = pr / p.k;
+          wgt = __int_as_float(
+              __ldg(p.blob + static_cast<size_t>(tk) * 2 * p.k + p.k + (pr - tk * p.k)));
+        }
+        wts[j] = wgt;
+      }
+      __syncwarp();
+    }
+    if (!mbar_wait(&s.tfull[acc], acc_phase, abort_flag)) {
+      record_error(p, abort_flag, MOE_ERR_TIMEOUT);
+      break;
+    }
+    tc_fence_after();
+    const uint32_t tbase =
+        tmem_base + static_cast<uint32_t>(acc * BN_MAX) + (static_cast<uint32_t>(sp * 32) << 16);
+    for (int c0 = 0; c0 < t.bn; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), r);
+      tmem_wait_ld();
+      if (p.op == kOpGateUp) {
+        // lanes 0-15 hold gate rows, lanes 16-31 the up rows of the same 16
+        // features; lane < 16 finishes columns 0-7 of the chunk, lane >= 16
+        // columns 8-15.
+        const bool hi = lane >= 16;
+        float h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t send = hi ? r[i] : r[i + 8];
+          const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
+          const float g = hi ? other : __uint_as_float(r[i]);
+          const float u = hi ? __uint_as_float(r[i + 8]) : other;
+          h[i] = silu_f(g) * u;
+        }
+        const int f = t.m * 64 + 16 * sp + (lane & 15);
+        const int cbase = c0 + (hi ? 8 : 0);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(t.shared ? p.out_s : p.out);
+        const int ld = t.shared ? p.ld_out_s : p.ld_out;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int col = cbase + i;
+          if (col < t.n_valid)
+            out[static_cast<size_t>(t.b_row + col) * ld + f] = __float2bfloat16_rn(h[i]);
+        }
+      } else {
+        const int f = t.m * kBM + sp * 32 + lane;
+        float* out = static_cast<float*>(t.shared ? p.out_s : p.out);
+        const int ld = t.shared ? p.ld_out_s : p.ld_out;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int col = c0 + i;
+          if (col < t.n_valid)
+            out[static_cast<size_t>(t.b_row + col) * ld + f] = wts[col] * __uint_as_float(r[i]);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.tempty[acc]);
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+}
+
+// Token tile of k-block kb: bn rows of 64 K in 16-row boxes (128-B swizzle).
+__device__ __forceinline__ void load_token_tile(uint8_t* dst, const CUtensorMap* mb, uint64_t* bar,
+                                                const TileInfo& t, int kb, uint64_t pol) {
+  for (int i = 0; i < t.bn / 16; ++i)
+    tma_load_2d(dst + i * 2048, mb, bar, kb * kBK, t.b_row + 16 * i, pol);
+}
+
+// ==========================================================================
+// bf16 weights
+// ==========================================================================
+template <int BN_MAX, int STAGES>
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                        const __grid_constant__ CUtensorMap tm_a_s,
+                        const __grid_constant__ CUtensorMap tm_b,
+                        const __grid_constant__ CUtensorMap tm_b_s, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  using Smem = Bf16Smem<BN_MAX, STAGES>;
+  const uint32_t raw = smem_u32(smem_raw);
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
+  GemmCommon<BN_MAX>& cm = s.c;
+  constexpr uint32_t kTmemCols = (2 * BN_MAX < 32) ? 32u : static_cast<uint32_t>(2 * BN_MAX);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.E + p.has_shared;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    init_common_barriers<BN_MAX>(cm);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_b);
+    if (p.has_shared) {
+      prefetch_tmap(&tm_a_s);
+      prefetch_tmap(&tm_b_s);
+    }
+  }
+  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kBaseThreads);
   if (warp == 1) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_alloc(&cm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int ntiles = s.tile_start[G];
-  const uint32_t tmem_base = s.tmem_base;
-  volatile int* abort_flag = &s.abort_flag;
+  const uint32_t tmem_base = cm.tmem_base;
+  volatile int* abort_flag = &cm.abort_flag;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -279,17 +387,190 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;  // bit i: stage i had a load issued; its phase in issued_ph
       uint32_t issued_ph = 0;
-      uint32_t tile_ctr = 0;  // W4A16 scale tables issued
-      uint32_t sissued = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-        const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
         const CUtensorMap* ma = t.shared ? &tm_a_s : &tm_a;
         const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
-        const uint32_t bytes = kABytes + static_cast<uint32_t>(t.bn) * 128u;
-        const int a_row0 = t.shared ? 0 : t.e * p.a_rows_per_expert;
-        if (Smem::kScaleTab && p.scale_table) {
-          // this tile's group scales: 128 rows x K/128 groups, same row order as the weights
+        const uint32_t bytes = kAStage + static_cast<uint32_t>(t.bn) * 128u;
+        const int row = tile_a_row(p, t);
+        for (int kb = 0; kb < t.k_blocks; ++kb) {
+          if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.full[stage], bytes);
+          issued |= 1u << stage;
+          issued_ph = (issued_ph & ~(1u << stage)) | (phase << stage);
+          if (p.op == kOpGateUp) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              tma_load_3d(s.a[stage] + b * 4096, ma, &s.full[stage], kb * kBK, row + 16 * b, 0,
+                          pol_w);
+          } else {
+            tma_load_2d(s.a[stage], ma, &s.full[stage], kb * kBK, row, pol_w);
+          }
+          load_token_tile(s.b[stage], mb, &s.full[stage], t, kb, pol_x);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_error(p, abort_flag, MOE_ERR_TIMEOUT);
+        for (int i = 0; i < STAGES; ++i)
+          if ((issued >> i) & 1u) mbar_wait_time_only(&s.full[i], (issued_ph >> i) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+        if (!mbar_wait(&cm.tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN_MAX);
+        const uint32_t idesc = idesc_bf16_f32(kBM, t.bn);
+        for (int kb = 0; kb < t.k_blocks; ++kb) {
+          if (!mbar_wait(&s.full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(s.a[stage]));
+          const uint64_t bd = sdesc_sw128(smem_u32(s.b[stage]));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(&s.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&cm.tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
+      // No MMA may be in flight when TMEM is released.
+      mma_commit(&cm.drain);
+      mbar_wait_time_only(&cm.drain, 0);
+    }
+  } else {
+    epilogue_role<BN_MAX>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ==========================================================================
+// W4A16 weights: packed int4 restored to bf16 in shared memory ahead of the MMA
+// ==========================================================================
+//   producer (warp 0): per tile, the tile's group-scale table (TMA, double
+//             buffered, when scale_table is set); per packed stage (4 k-blocks),
+//             128 rows x 128 B of packed int4 (128-B swizzle).
+//   token producer (warp 14): per k-block, the token tile.  A separate thread,
+//             so the weight ring prefetches to its full depth (64 KB) no matter
+//             how far the token ring is filled.
+//   dequant group g (warps 6+4g .. 9+4g): for every packed stage, restores
+//             k-blocks 4q + g and 4q + 2 + g (those that exist) into operand
+//             buffers 2g and 2g + 1, then releases the packed stage.  Every
+//             group consumes every packed stage and only its own buffers, so
+//             all waits stay in phase order, and the MMA of one buffer overlaps
+//             the restore of the other.
+//   MMA:      per k-block 4q + j, operand buffer 2 (j % 2) + j / 2 and the next
+//             token stage.
+template <int BN_MAX, int PSTAGES, int BSTAGES>
+__global__ void __launch_bounds__(kW4Threads, 1)
+    grouped_gemm_w4_kernel(const __grid_constant__ CUtensorMap tm_a,
+                           const __grid_constant__ CUtensorMap tm_a_s,
+                           const __grid_constant__ CUtensorMap tm_b,
+                           const __grid_constant__ CUtensorMap tm_b_s,
+                           const __grid_constant__ CUtensorMap tm_sc,
+                           const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  using Smem = W4Smem<BN_MAX, PSTAGES, BSTAGES>;
+  const uint32_t raw = smem_u32(smem_raw);
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
+  GemmCommon<BN_MAX>& cm = s.c;
+  constexpr uint32_t kTmemCols = (2 * BN_MAX < 32) ? 32u : static_cast<uint32_t>(2 * BN_MAX);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.E + p.has_shared;
+  const bool table = p.scale_table != 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < PSTAGES; ++i) {
+      mbar_init(&s.pfull[i], 1);
+      mbar_init(&s.pempty[i], kDequantWarps);
+    }
+    for (int i = 0; i < BSTAGES; ++i) {
+      mbar_init(&s.bfull[i], 1);
+      mbar_init(&s.bempty[i], 1);
+    }
+    for (int i = 0; i < kABuffers; ++i) {
+      mbar_init(&s.aready[i], kWarpsPerGroup);
+      mbar_init(&s.afree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.sfull[i], 1);
+      mbar_init(&s.sempty[i], kDequantWarps);
+    }
+    init_common_barriers<BN_MAX>(cm);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_b);
+    if (table) prefetch_tmap(&tm_sc);
+    if (p.has_shared) {
+      prefetch_tmap(&tm_a_s);
+      prefetch_tmap(&tm_b_s);
+      if (table) prefetch_tmap(&tm_sc_s);
+    }
+  }
+  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kW4Threads);
+  if (warp == 1) {
+    tmem_alloc(&cm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = cm.tmem_base;
+  volatile int* abort_flag = &cm.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer: weights
+      const uint64_t pol_w = policy_evict_first();
+      int ps = 0;
+      uint32_t pph = 0;
+      uint32_t tile_ctr = 0;
+      // loads in flight on abort: packed stages (bit, phase) and the last table
+      uint32_t p_iss = 0, p_issph = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+        const CUtensorMap* ma = t.shared ? &tm_a_s : &tm_a;
+        const int row = tile_a_row(p, t);
+        if (table) {
           const int sb = tile_ctr & 1;
           if (!mbar_wait(&s.sempty[sb], ((tile_ctr >> 1) & 1u) ^ 1u, abort_flag)) {
             ok = false;
@@ -301,49 +582,42 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
           if (p.op == kOpGateUp) {
 #pragma unroll
             for (int b = 0; b < 4; ++b)
-              tma_load_3d(s.stab[sb] + b * 32 * ngrp, msc, &s.sfull[sb], 0,
-                          a_row0 + t.m * 64 + 16 * b, 0, pol_w);
+              tma_load_3d(s.stab[sb] + b * 32 * ngrp, msc, &s.sfull[sb], 0, row + 16 * b, 0,
+                          pol_w);
           } else {
-            tma_load_2d(s.stab[sb], msc, &s.sfull[sb], 0, a_row0 + t.m * kBM, pol_w);
+            tma_load_2d(s.stab[sb], msc, &s.sfull[sb], 0, row, pol_w);
           }
-          sissued = 1u << sb;
           ++tile_ctr;
         }
-        for (int kb = 0; kb < t.k_blocks; ++kb) {
-          if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&s.full[stage], bytes);
-          issued |= 1u << stage;
-          issued_ph = (issued_ph & ~(1u << stage)) | (phase << stage);
-          const int kc = kb * kBK;
-          // weights: bf16 tiles at column kc, or packed int4 at word kc / 8
-          void* adst = QUANT ? static_cast<void*>(s.araw[stage]) : static_cast<void*>(s.a[stage]);
-          const int ac = QUANT ? kc / 8 : kc;
-          constexpr int kRowBytes = QUANT ? kBK / 2 : kBK * 2;
-          if (p.op == kOpGateUp) {
-            const int row = a_row0 + t.m * 64;
+        for (int kb = 0; kb < t.k_blocks; kb += kKPerPacked) {
+          {
+            if (!mbar_wait(&s.pempty[ps], pph ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&s.pfull[ps], kPackedStage);
+            p_iss |= 1u << ps;
+            p_issph = (p_issph & ~(1u << ps)) | (pph << ps);
+            const int wc = kb * kBK / 8;  // packed words along K
+            if (p.op == kOpGateUp) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-              tma_load_3d(static_cast<uint8_t*>(adst) + b * 32 * kRowBytes, ma, &s.full[stage], ac,
-                          row + 16 * b, 0, pol_w);
-          } else {
-            tma_load_2d(adst, ma, &s.full[stage], ac, a_row0 + t.m * kBM, pol_w);
-          }
-          for (int i = 0; i < t.bn / 16; ++i)
-            tma_load_2d(s.b[stage] + i * 2048, mb, &s.full[stage], kc, t.b_row + 16 * i, pol_x);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+              for (int b = 0; b < 4; ++b)
+                tma_load_3d(s.praw[ps] + b * 4096, ma, &s.pfull[ps], wc, row + 16 * b, 0, pol_w);
+            } else {
+              tma_load_2d(s.praw[ps], ma, &s.pfull[ps], wc, row, pol_w);
+            }
+            if (++ps == PSTAGES) {
+              ps = 0;
+              pph ^= 1u;
+            }
           }
         }
       }
       if (!ok) {
         record_error(p, abort_flag, MOE_ERR_TIMEOUT);
-        for (int i = 0; i < STAGES; ++i)
-          if ((issued >> i) & 1u) mbar_wait_time_only(&s.full[i], (issued_ph >> i) & 1u);
-        if (sissued) {
+        for (int i = 0; i < PSTAGES; ++i)
+          if ((p_iss >> i) & 1u) mbar_wait_time_only(&s.pfull[i], (p_issph >> i) & 1u);
+        if (tile_ctr > 0) {
           const uint32_t last = tile_ctr - 1;
           mbar_wait_time_only(&s.sfull[last & 1], (last >> 1) & 1u);
         }
@@ -352,16 +626,15 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0;
-      int abuf = 0;  // W4A16: restored operand buffer and its phase
-      uint32_t aphase = 0;
+      int bs = 0;
+      uint32_t bph = 0;
+      uint32_t aph = 0;  // bit g: phase of operand buffer g
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-        const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
-        if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, abort_flag)) {
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+        if (!mbar_wait(&cm.tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -369,188 +642,135 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN_MAX);
         const uint32_t idesc = idesc_bf16_f32(kBM, t.bn);
         for (int kb = 0; kb < t.k_blocks; ++kb) {
-          if ((QUANT && !mbar_wait(&s.aready[abuf], aphase, abort_flag)) ||
-              !mbar_wait(&s.full[stage], phase, abort_flag)) {
+          // k-block 4q + j sits in buffer 2 (j % 2) + j / 2 (group j % 2)
+          const int j = kb % kKPerPacked;
+          const int g = 2 * (j % 2) + j / 2;
+          if (!mbar_wait(&s.aready[g], (aph >> g) & 1u, abort_flag) ||
+              !mbar_wait(&s.bfull[bs], bph, abort_flag)) {
             ok = false;
             break;
           }
+          aph ^= 1u << g;
           tc_fence_after();
-          const uint64_t ad = sdesc_sw128(smem_u32(s.a[QUANT ? abuf : stage]));
-          const uint64_t bd = sdesc_sw128(smem_u32(s.b[stage]));
+          const uint64_t ad = sdesc_sw128(smem_u32(s.a[g]));
+          const uint64_t bd = sdesc_sw128(smem_u32(s.b[bs]));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-          mma_commit(&s.empty[stage]);
-          if (QUANT) {
-            mma_commit(&s.afree[abuf]);
-            if (++abuf == Smem::kA) {
-              abuf = 0;
-              aphase ^= 1u;
-            }
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          mma_commit(&s.bempty[bs]);
+          mma_commit(&s.afree[g]);
+          if (++bs == BSTAGES) {
+            bs = 0;
+            bph ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&s.tfull[acc]);
+        mma_commit(&cm.tfull[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
-      // No MMA may be in flight when TMEM is released.
-      mma_commit(&s.drain);
-      mbar_wait_time_only(&s.drain, 0);
+      mma_commit(&cm.drain);
+      mbar_wait_time_only(&cm.drain, 0);
     }
   } else if (warp < 6) {
-    // -------------------------------------------------- epilogue (warps 2-5)
-    const int sp = warp & 3;  // TMEM lanes 32*sp .. 32*sp+31
-    float* wts = s.row_weight[warp - 2];
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int L = blockIdx.x; L < ntiles; L += gridDim.x) {
-      const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
-      if (p.op == kOpDown) {
-        // Routing weight of every token row of the tile, fetched before the
-        // accumulator is ready: row r holds pair p = perm_pair[r] (token p / k,
-        // slot p % k); the shared group has weight 1.
-        __syncwarp();
-        for (int j = lane; j < t.n_valid; j += 32) {
-          float wgt = 1.0f;
-          if (!t.shared) {
-            const int pr = __ldg(p.perm_pair + t.b_row + j);
-            const int tk = pr / p.k;
-            wgt = __int_as_float(
-                __ldg(p.blob + static_cast<size_t>(tk) * 2 * p.k + p.k + (pr - tk * p.k)));
+    epilogue_role<BN_MAX>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
+  } else if (warp == kTokenWarp) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer: token tiles
+      const uint64_t pol_x = policy_evict_last();
+      int bs = 0;
+      uint32_t bph = 0;
+      uint32_t b_iss = 0, b_issph = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+        const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
+        for (int kb = 0; kb < t.k_blocks; ++kb) {
+          if (!mbar_wait(&s.bempty[bs], bph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
           }
-          wts[j] = wgt;
+          mbar_arrive_expect_tx(&s.bfull[bs], static_cast<uint32_t>(t.bn) * 128u);
+          b_iss |= 1u << bs;
+          b_issph = (b_issph & ~(1u << bs)) | (bph << bs);
+          load_token_tile(s.b[bs], mb, &s.bfull[bs], t, kb, pol_x);
+          if (++bs == BSTAGES) {
+            bs = 0;
+            bph ^= 1u;
+          }
         }
-        __syncwarp();
       }
-      if (!mbar_wait(&s.tfull[acc], acc_phase, abort_flag)) {
+      if (!ok) {
         record_error(p, abort_flag, MOE_ERR_TIMEOUT);
-        break;
+        for (int i = 0; i < BSTAGES; ++i)
+          if ((b_iss >> i) & 1u) mbar_wait_time_only(&s.bfull[i], (b_issph >> i) & 1u);
       }
-      tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + static_cast<uint32_t>(acc * BN_MAX) + (static_cast<uint32_t>(sp * 32) << 16);
-      for (int c0 = 0; c0 < t.bn; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), r);
-        tmem_wait_ld();
-        if (p.op == kOpGateUp) {
-          // lanes 0-15 hold gate rows, lanes 16-31 the up rows of the same 16
-          // features; lane < 16 finishes columns 0-7 of the chunk, lane >= 16
-          // columns 8-15.
-          const bool hi = lane >= 16;
-          float h[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t send = hi ? r[i] : r[i + 8];
-            const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
-            const float g = hi ? other : __uint_as_float(r[i]);
-            const float u = hi ? __uint_as_float(r[i + 8]) : other;
-            h[i] = silu_f(g) * u;
-          }
-          const int f = t.m * 64 + 16 * sp + (lane & 15);
-          const int cbase = c0 + (hi ? 8 : 0);
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(t.shared ? p.out_s : p.out);
-          const int ld = t.shared ? p.ld_out_s : p.ld_out;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = cbase + i;
-            if (col < t.n_valid)
-              out[static_cast<size_t>(t.b_row + col) * ld + f] = __float2bfloat16_rn(h[i]);
-          }
-        } else {
-          const int f = t.m * kBM + sp * 32 + lane;
-          float* out = static_cast<float*>(t.shared ? p.out_s : p.out);
-          const int ld = t.shared ? p.ld_out_s : p.ld_out;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c0 + i;
-            if (col < t.n_valid)
-              out[static_cast<size_t>(t.b_row + col) * ld + f] = wts[col] * __uint_as_float(r[i]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
     }
-  } else if (QUANT) {
-    // -------------------------------------------------- dequant (warps 6-13, W4A16)
-    // kDequantGroups groups of kWarpsPerGroup warps.  The running k-block index
-    // i goes to group i mod kDequantGroups; since the raw ring depth and the
-    // operand ring depth are both multiples of the group count, every raw stage
-    // and every operand buffer always belongs to the same group, so each group
-    // waits on each of its barriers in phase order.  Within a group, thread tg
-    // owns tile rows tg + 64 j: it reads the row's 32 B of packed int4 and writes
-    // eight 16-B chunks of bf16 into the 128-B-swizzled operand tile (chunk c of
-    // row r lives at r*128 + ((c ^ (r & 7)) << 4)).
-    constexpr int kGroupThreads = 32 * kWarpsPerGroup;
-    constexpr int kRowsPerThread = kBM / kGroupThreads;
-    static_assert(STAGES % kDequantGroups == 0, "raw stages must map to fixed groups");
+  } else {
+    // -------------------------------------------------- dequant groups
+    // Thread r of group grp owns tile row r.  In a packed stage (128-B swizzled
+    // rows of 256 int4 values) k-block j of the stage is 16-B chunks 2j, 2j + 1
+    // of each row; the thread writes eight 16-B bf16 chunks into the
+    // 128-B-swizzled operand buffer (chunk c of row r at r*128 + ((c ^ (r & 7)) << 4)).
     const int dw = warp - 6;
     const int grp = dw / kWarpsPerGroup;
-    const int tg = (dw % kWarpsPerGroup) * 32 + lane;
-    uint32_t idx = 0;  // running k-block index (the same sequence every role walks)
+    const int r = (dw % kWarpsPerGroup) * 32 + lane;
+    int ps = 0;
+    uint32_t pph = 0;
+    uint32_t aphase = 0;  // bit h: phase of this group's buffer 2 grp + h
     uint32_t tile_ctr = 0;
-    const bool table = Smem::kScaleTab && p.scale_table;
     bool ok = true;
     for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-      const TileInfo t = decode_tile<Smem, BN_MAX>(s, p, G, L);
+      const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
       const int K = t.shared ? p.K_s : p.K;
       const int ngrp = K / p.group;
-      const uint16_t* sbase = t.shared ? p.wscale_s : p.wscale;
-      const uint16_t* srow[kRowsPerThread];
-#pragma unroll
-      for (int j = 0; j < kRowsPerThread; ++j)
-        srow[j] = sbase + static_cast<size_t>(tile_weight_row(p, t, tg + j * kGroupThreads)) * ngrp;
+      const uint16_t* srow = (t.shared ? p.wscale_s : p.wscale) +
+                             static_cast<size_t>(tile_weight_row(p, t, r)) * ngrp;
       const int sb = tile_ctr & 1;
       if (table && !mbar_wait(&s.sfull[sb], (tile_ctr >> 1) & 1u, abort_flag)) {
         ok = false;
         break;
       }
-      for (int kb = 0; kb < t.k_blocks; ++kb, ++idx) {
-        if (static_cast<int>(idx % kDequantGroups) != grp) continue;
-        const int stage = static_cast<int>(idx % STAGES);
-        const uint32_t phase = (idx / STAGES) & 1u;
-        const int abuf = static_cast<int>(idx % kABufs);
-        const uint32_t aphase = (idx / kABufs) & 1u;
-        __nv_bfloat162 s2[kRowsPerThread];
-#pragma unroll
-        for (int j = 0; j < kRowsPerThread; ++j) {
-          const int g = (kb * kBK) / p.group;
-          const uint16_t sbits = table ? s.stab[sb][(tg + j * kGroupThreads) * ngrp + g]
-                                       : __ldg(srow[j] + g);
-          s2[j].x = __ushort_as_bfloat16(sbits);
-          s2[j].y = s2[j].x;
-        }
-        if (!mbar_wait(&s.full[stage], phase, abort_flag) ||
-            !mbar_wait(&s.afree[abuf], aphase ^ 1u, abort_flag)) {
+      for (int kb0 = 0; kb0 < t.k_blocks && ok; kb0 += kKPerPacked) {
+        if (!mbar_wait(&s.pfull[ps], pph, abort_flag)) {
           ok = false;
           break;
         }
+        const uint8_t* prow = s.praw[ps] + r * 128;
 #pragma unroll
-        for (int j = 0; j < kRowsPerThread; ++j) {
-          const int r = tg + j * kGroupThreads;
-          const uint4 p0 = *reinterpret_cast<const uint4*>(s.araw[stage] + r * 32);
-          const uint4 p1 = *reinterpret_cast<const uint4*>(s.araw[stage] + r * 32 + 16);
+        for (int h = 0; h < 2; ++h) {
+          const int j = 2 * h + grp;  // k-block within the packed stage
+          const int kb = kb0 + j;
+          if (kb >= t.k_blocks) continue;
+          const int buf = 2 * grp + h;
+          const int g = (kb * kBK) / p.group;
+          const uint16_t sbits = table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
+          __nv_bfloat162 s2;
+          s2.x = __ushort_as_bfloat16(sbits);
+          s2.y = s2.x;
+          const uint4 p0 = *reinterpret_cast<const uint4*>(prow + (((2 * j) ^ (r & 7)) << 4));
+          const uint4 p1 = *reinterpret_cast<const uint4*>(prow + (((2 * j + 1) ^ (r & 7)) << 4));
           const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          uint8_t* arow = s.a[abuf] + r * 128;
+          if (!mbar_wait(&s.afree[buf], ((aphase >> h) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* arow = s.a[buf] + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(words[c], s2[j]);
+            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(words[c], s2);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.aready[buf]);
+          aphase ^= 1u << h;
         }
-        fence_proxy_async_smem();
+        if (!ok) break;
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&s.aready[abuf]);
-          mbar_arrive(&s.empty[stage]);
+        if (lane == 0) mbar_arrive(&s.pempty[ps]);
+        if (++ps == PSTAGES) {
+          ps = 0;
+          pph ^= 1u;
         }
       }
       if (!ok) break;
@@ -571,26 +791,373 @@ __global__ void __launch_bounds__(GemmRoles<QUANT>::kThreads, 1)
   }
 }
 
-template <int BN_MAX, int STAGES, int QUANT>
-static cudaError_t launch_variant(const GemmParams& p, const GemmMaps& m, int num_sms,
-                                  cudaStream_t st) {
-  const size_t smem = sizeof(GemmSmem<BN_MAX, STAGES, QUANT>) + 1024;
-  auto kern = grouped_gemm_kernel<BN_MAX, STAGES, QUANT>;
+// ==========================================================================
+// W4A16 weights, restored operand in tensor memory (token tiles up to 64 rows)
+// ==========================================================================
+// The eight dequant warps write restored bf16 weight rows straight into TMEM
+// with tcgen05.st (thread = tile row = TMEM lane, two K values per 32-bit
+// column), and the MMA reads A from TMEM.  TMEM holds the double-buffered
+// accumulators (2 x 64 columns) and kTmemABufs operand buffers of 32 columns
+// (one k-block each), so restoring runs up to kTmemABufs k-blocks ahead of the
+// MMA.  Dequant warp w serves TMEM lane quarter w % 4 and the k-blocks j of a
+// packed stage with j % 2 == (w - 6) / 4; k-block index i (running over the
+// CTA's tiles, aligned to packed stages) uses buffer i % kTmemABufs, and since
+// kTmemABufs is a multiple of 4 every buffer is always written by the same
+// four warps.
+constexpr int kTmemABufs = 12;
+constexpr uint32_t kTmemAccCols = 128;  // 2 x 64 accumulator columns
+static_assert(kTmemABufs % kKPerPacked == 0, "buffers must map to fixed warps");
+static_assert(kTmemAccCols + 32 * kTmemABufs <= 512, "TMEM budget");
+
+template <int PSTAGES, int BSTAGES>
+struct W4TSmem {
+  uint8_t b[BSTAGES][64 * 128];         // token rows per k-block
+  uint8_t praw[PSTAGES][kPackedStage];  // packed int4 rows, 128-B swizzle
+  uint16_t stab[2][kScaleTabElems];     // group scales of the current tiles
+  uint64_t pfull[PSTAGES], pempty[PSTAGES];
+  uint64_t bfull[BSTAGES], bempty[BSTAGES];
+  uint64_t aready[kTmemABufs], afree[kTmemABufs];
+  uint64_t sfull[2], sempty[2];
+  GemmCommon<64> c;
+};
+
+template <int PSTAGES, int BSTAGES>
+__global__ void __launch_bounds__(kW4Threads, 1)
+    grouped_gemm_w4t_kernel(const __grid_constant__ CUtensorMap tm_a,
+                            const __grid_constant__ CUtensorMap tm_a_s,
+                            const __grid_constant__ CUtensorMap tm_b,
+                            const __grid_constant__ CUtensorMap tm_b_s,
+                            const __grid_constant__ CUtensorMap tm_sc,
+                            const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
+  constexpr int BN_MAX = 64;
+  extern __shared__ uint8_t smem_raw[];
+  using Smem = W4TSmem<PSTAGES, BSTAGES>;
+  const uint32_t raw = smem_u32(smem_raw);
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
+  GemmCommon<BN_MAX>& cm = s.c;
+  constexpr uint32_t kTmemCols = 512;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.E + p.has_shared;
+  const bool table = p.scale_table != 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < PSTAGES; ++i) {
+      mbar_init(&s.pfull[i], 1);
+      mbar_init(&s.pempty[i], kDequantWarps);
+    }
+    for (int i = 0; i < BSTAGES; ++i) {
+      mbar_init(&s.bfull[i], 1);
+      mbar_init(&s.bempty[i], 1);
+    }
+    for (int i = 0; i < kTmemABufs; ++i) {
+      mbar_init(&s.aready[i], 4);  // one warp per TMEM lane quarter
+      mbar_init(&s.afree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.sfull[i], 1);
+      mbar_init(&s.sempty[i], kDequantWarps);
+    }
+    init_common_barriers<BN_MAX>(cm);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_b);
+    if (table) prefetch_tmap(&tm_sc);
+    if (p.has_shared) {
+      prefetch_tmap(&tm_a_s);
+      prefetch_tmap(&tm_b_s);
+      if (table) prefetch_tmap(&tm_sc_s);
+    }
+  }
+  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kW4Threads);
+  if (warp == 1) {
+    tmem_alloc(&cm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = cm.tmem_base;
+  volatile int* abort_flag = &cm.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer: weights + scales
+      const uint64_t pol_w = policy_evict_first();
+      int ps = 0;
+      uint32_t pph = 0;
+      uint32_t tile_ctr = 0;
+      uint32_t p_iss = 0, p_issph = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+        const CUtensorMap* ma = t.shared ? &tm_a_s : &tm_a;
+        const int row = tile_a_row(p, t);
+        if (table) {
+          const int sb = tile_ctr & 1;
+          if (!mbar_wait(&s.sempty[sb], ((tile_ctr >> 1) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int ngrp = (t.shared ? p.K_s : p.K) / p.group;
+          const CUtensorMap* msc = t.shared ? &tm_sc_s : &tm_sc;
+          mbar_arrive_expect_tx(&s.sfull[sb], static_cast<uint32_t>(kBM * ngrp * 2));
+          if (p.op == kOpGateUp) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              tma_load_3d(s.stab[sb] + b * 32 * ngrp, msc, &s.sfull[sb], 0, row + 16 * b, 0,
+                          pol_w);
+          } else {
+            tma_load_2d(s.stab[sb], msc, &s.sfull[sb], 0, row, pol_w);
+          }
+          ++tile_ctr;
+        }
+        for (int kb = 0; kb < t.k_blocks; kb += kKPerPacked) {
+          if (!mbar_wait(&s.pempty[ps], pph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.pfull[ps], kPackedStage);
+          p_iss |= 1u << ps;
+          p_issph = (p_issph & ~(1u << ps)) | (pph << ps);
+          const int wc = kb * kBK / 8;
+          if (p.op == kOpGateUp) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              tma_load_3d(s.praw[ps] + b * 4096, ma, &s.pfull[ps], wc, row + 16 * b, 0, pol_w);
+          } else {
+            tma_load_2d(s.praw[ps], ma, &s.pfull[ps], wc, row, pol_w);
+          }
+          if (++ps == PSTAGES) {
+            ps = 0;
+            pph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_error(p, abort_flag, MOE_ERR_TIMEOUT);
+        for (int i = 0; i < PSTAGES; ++i)
+          if ((p_iss >> i) & 1u) mbar_wait_time_only(&s.pfull[i], (p_issph >> i) & 1u);
+        if (tile_ctr > 0) {
+          const uint32_t last = tile_ctr - 1;
+          mbar_wait_time_only(&s.sfull[last & 1], (last >> 1) & 1u);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer (A from TMEM)
+      int bs = 0;
+      uint32_t bph = 0;
+      uint32_t idx = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+        if (!mbar_wait(&cm.tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN_MAX);
+        const uint32_t idesc = idesc_bf16_f32(kBM, t.bn);
+        for (int kb = 0; kb < t.k_blocks; ++kb, ++idx) {
+          const int buf = static_cast<int>(idx % kTmemABufs);
+          if (!mbar_wait(&s.aready[buf], (idx / kTmemABufs) & 1u, abort_flag) ||
+              !mbar_wait(&s.bfull[bs], bph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem_base + kTmemAccCols + 32u * buf;
+          const uint64_t bd = sdesc_sw128(smem_u32(s.b[bs]));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ts(d_tmem, a_tmem + 8u * kk, bd + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(&s.bempty[bs]);
+          mma_commit(&s.afree[buf]);
+          if (++bs == BSTAGES) {
+            bs = 0;
+            bph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&cm.tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
+      mma_commit(&cm.drain);
+      mbar_wait_time_only(&cm.drain, 0);
+    }
+  } else if (warp < 6) {
+    epilogue_role<BN_MAX>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
+  } else if (warp == kTokenWarp) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer: token tiles
+      const uint64_t pol_x = policy_evict_last();
+      int bs = 0;
+      uint32_t bph = 0;
+      uint32_t b_iss = 0, b_issph = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+        const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+        const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
+        for (int kb = 0; kb < t.k_blocks; ++kb) {
+          if (!mbar_wait(&s.bempty[bs], bph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.bfull[bs], static_cast<uint32_t>(t.bn) * 128u);
+          b_iss |= 1u << bs;
+          b_issph = (b_issph & ~(1u << bs)) | (bph << bs);
+          load_token_tile(s.b[bs], mb, &s.bfull[bs], t, kb, pol_x);
+          if (++bs == BSTAGES) {
+            bs = 0;
+            bph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_error(p, abort_flag, MOE_ERR_TIMEOUT);
+        for (int i = 0; i < BSTAGES; ++i)
+          if ((b_iss >> i) & 1u) mbar_wait_time_only(&s.bfull[i], (b_issph >> i) & 1u);
+      }
+    }
+  } else {
+    // -------------------------------------------------- dequant warps -> TMEM
+    const int qd = warp & 3;                 // TMEM lane quarter
+    const int hd = (warp - 6) / 4;           // k-blocks j with j % 2 == hd
+    const int r = 32 * qd + lane;            // tile row == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
+    int ps = 0;
+    uint32_t pph = 0;
+    uint32_t idx = 0;  // running k-block index, aligned to packed stages
+    uint32_t tile_ctr = 0;
+    bool ok = true;
+    for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+      const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
+      const int K = t.shared ? p.K_s : p.K;
+      const int ngrp = K / p.group;
+      const uint16_t* srow = (t.shared ? p.wscale_s : p.wscale) +
+                             static_cast<size_t>(tile_weight_row(p, t, r)) * ngrp;
+      const int sb = tile_ctr & 1;
+      if (table && !mbar_wait(&s.sfull[sb], (tile_ctr >> 1) & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      for (int kb0 = 0; kb0 < t.k_blocks && ok; kb0 += kKPerPacked, idx += kKPerPacked) {
+        if (!mbar_wait(&s.pfull[ps], pph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* prow = s.praw[ps] + r * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = 2 * h + hd;  // k-block within the packed stage
+          const uint32_t i = idx + j;
+          const int buf = static_cast<int>(i % kTmemABufs);
+          const int g = ((kb0 + j) * kBK) / p.group;
+          const uint16_t sbits = table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
+          __nv_bfloat162 s2;
+          s2.x = __ushort_as_bfloat16(sbits);
+          s2.y = s2.x;
+          const uint4 p0 = *reinterpret_cast<const uint4*>(prow + (((2 * j) ^ (r & 7)) << 4));
+          const uint4 p1 = *reinterpret_cast<const uint4*>(prow + (((2 * j + 1) ^ (r & 7)) << 4));
+          const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 q = dequant_word(words[c], s2);
+            v[4 * c] = q.x;
+            v[4 * c + 1] = q.y;
+            v[4 * c + 2] = q.z;
+            v[4 * c + 3] = q.w;
+          }
+          if (!mbar_wait(&s.afree[buf], ((i / kTmemABufs) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_st_32x32b_x32(tmem_base + lane_addr + kTmemAccCols + 32u * buf, v);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.aready[buf]);
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.pempty[ps]);
+        if (++ps == PSTAGES) {
+          ps = 0;
+          pph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (table) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sempty[sb]);
+        ++tile_ctr;
+      }
+    }
+    if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BN_MAX, int STAGES>
+static cudaError_t launch_bf16(const GemmParams& p, const GemmMaps& m, int num_sms,
+                               cudaStream_t st) {
+  const size_t smem = sizeof(Bf16Smem<BN_MAX, STAGES>) + 1024;
+  auto kern = grouped_gemm_kernel<BN_MAX, STAGES>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, GemmRoles<QUANT>::kThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
+  kern<<<num_sms, kBaseThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, p);
+  return cudaGetLastError();
+}
+
+template <int BN_MAX, int PSTAGES, int BSTAGES>
+static cudaError_t launch_w4(const GemmParams& p, const GemmMaps& m, int num_sms,
+                             cudaStream_t st) {
+  const size_t smem = sizeof(W4Smem<BN_MAX, PSTAGES, BSTAGES>) + 1024;
+  auto kern = grouped_gemm_w4_kernel<BN_MAX, PSTAGES, BSTAGES>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kW4Threads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
+  return cudaGetLastError();
+}
+
+template <int PSTAGES, int BSTAGES>
+static cudaError_t launch_w4t(const GemmParams& p, const GemmMaps& m, int num_sms,
+                              cudaStream_t st) {
+  const size_t smem = sizeof(W4TSmem<PSTAGES, BSTAGES>) + 1024;
+  auto kern = grouped_gemm_w4t_kernel<PSTAGES, BSTAGES>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kW4Threads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int bn_max, int quant,
                                 int num_sms, cudaStream_t st) {
   if (quant == 0) {
-    if (bn_max == 64) return launch_variant<64, 8, 0>(p, maps, num_sms, st);
-    if (bn_max == 256) return launch_variant<256, 4, 0>(p, maps, num_sms, st);
+    if (bn_max == 64) return launch_bf16<64, 8>(p, maps, num_sms, st);
+    if (bn_max == 256) return launch_bf16<256, 4>(p, maps, num_sms, st);
   } else if (quant == 1) {
-    if (bn_max == 64) return launch_variant<64, 8, 1>(p, maps, num_sms, st);
-    if (bn_max == 256) return launch_variant<256, 4, 1>(p, maps, num_sms, st);
+    if (bn_max == 64) return launch_w4t<4, 12>(p, maps, num_sms, st);
+    if (bn_max == 256) return launch_w4<256, 3, 2>(p, maps, num_sms, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -107,32 +107,32 @@ bool map_gate_up_bf16(CUtensorMap* m, const void* base, uint64_t groups, uint64_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Packed int4 weights [rows][cols/8] int32 (no swizzle): 2-D map with a
-// {8 words = 64 values, box_rows} box.
+// Packed int4 weights [rows][cols/8] int32: 2-D map with a {32 words = 256
+// values = 128 B, box_rows} box and the 128-byte swizzle.
 bool map_2d_i4(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cols / 8, rows};
   const cuuint64_t strides[1] = {cols / 2};
-  const cuuint32_t box[2] = {8, box_rows};
+  const cuuint32_t box[2] = {32, box_rows};
   const cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Packed int4 gate/up weights [groups][2*half][cols/8]: the 3-D gate/up pairing
-// of map_gate_up_bf16 with a {8 words, 16, 2} box.
+// of map_gate_up_bf16 with a {32 words, 16, 2} box and the 128-byte swizzle.
 bool map_gate_up_i4(CUtensorMap* m, const void* base, uint64_t groups, uint64_t half,
                     uint64_t cols) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {cols / 8, groups * 2 * half, 2};
   const cuuint64_t strides[2] = {cols / 2, half * (cols / 2)};
-  const cuuint32_t box[3] = {8, 16, 2};
+  const cuuint32_t box[3] = {32, 16, 2};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -173,8 +173,10 @@ int validate(const moe_config* c) {
     if (c->I % 64 != 0 || c->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
   } else if (c->quant == MOE_QUANT_W4A16) {
     // symmetric int4, group 128 along K only (other layouts are rejected, as
-    // unsupported quantisation formats are rejected at model load)
-    if (c->group != 128 || c->I % 128 != 0 || c->I_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    // unsupported quantisation formats are rejected at model load); K tiles of
+    // 256 packed values: D, I and I_shared multiples of 256
+    if (c->group != 128 || c->D % 256 != 0 || c->I % 256 != 0 || c->I_shared % 256 != 0)
+      return MOE_ERR_UNSUPPORTED;
   } else {
     return MOE_ERR_UNSUPPORTED;
   }

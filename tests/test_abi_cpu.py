@@ -68,6 +68,12 @@ def test_w4a16_group_must_be_128(lib):
     assert lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_FORWARD) == 0
 
 
+def test_w4a16_needs_whole_packed_k_tiles(lib):
+    cfg = B.config(CONFIGS["w4a16"])
+    cfg.I = 1024 + 128  # not a multiple of 256
+    assert lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_FORWARD) == 0
+
+
 def test_null_and_misaligned_pointers_rejected(lib):
     cfg = B.config(CONFIGS["tiny"])
     d = ctypes.c_void_p(4096)

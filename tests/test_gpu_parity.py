@@ -35,11 +35,13 @@ SMALL = {
 
 # W4A16: symmetric int4 weights, group 128 along K, bf16 scales
 W4 = {
-    "w4_tiny": MoEConfig("w4_tiny", T=64, D=256, E=16, I=128, Is=128, k=2, quant=1),
-    "w4_ragged": MoEConfig("w4_ragged", T=37, D=384, E=24, I=256, Is=128, k=3, quant=1),
-    "w4_hot": MoEConfig("w4_hot", T=200, D=256, E=16, I=128, Is=256, k=2, quant=1, zipf_s=1.2,
+    "w4_tiny": MoEConfig("w4_tiny", T=64, D=256, E=16, I=256, Is=256, k=2, quant=1),
+    "w4_ragged": MoEConfig("w4_ragged", T=37, D=512, E=24, I=768, Is=256, k=3, quant=1),
+    "w4_hot": MoEConfig("w4_hot", T=200, D=256, E=16, I=256, Is=512, k=2, quant=1, zipf_s=1.2,
                         zipf_alpha=3.0),
-    "w4_wide": MoEConfig("w4_wide", T=2100, D=256, E=8, I=128, Is=128, k=2, quant=1),
+    "w4_wide": MoEConfig("w4_wide", T=2100, D=256, E=8, I=256, Is=256, k=2, quant=1),
+    # K = 1024 / 2048: exercises the TMA scale tables (K multiple of 1024)
+    "w4_table": MoEConfig("w4_table", T=96, D=2048, E=12, I=1024, Is=1024, k=3, quant=1),
 }
 
 
@@ -250,7 +252,7 @@ def test_forward_parity_w4a16(name):
     tol_check(y_host(y), ref)
 
 
-@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide"])
+@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide", "w4_table"])
 def test_grouped_gate_up_w4a16(name):
     cfg = W4[name]
     host, dev, ids, w, offsets, perm, inv, blob = grouped_setup(cfg)
@@ -276,7 +278,7 @@ def test_grouped_gate_up_w4a16(name):
     tol_check(y_host(hs), ref_s, what="h_shared")
 
 
-@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide"])
+@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide", "w4_table"])
 def test_grouped_down_w4a16(name):
     cfg = W4[name]
     host, dev, ids, w, offsets, perm, inv, blob = grouped_setup(cfg)
