@@ -162,7 +162,7 @@ __device__ float2 warp_dot_comp(const __nv_bfloat16* __restrict__ xr,
   float s = 0.f, c = 0.f;
   const uint4* xp = reinterpret_cast<const uint4*>(xr);
   const uint4* wp = reinterpret_cast<const uint4*>(wrow);
-#pragma unroll 4
+#pragma unroll 8
   for (int g = lane; g < D / 8; g += 32) {
     const uint4 xv = __ldg(xp + g), wv = __ldg(wp + g);
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -246,6 +246,10 @@ __device__ __forceinline__ bool better_d(double v, int e, double bv, int be) {
   return v > bv || (v == bv && e < be);
 }
 
+// One 256-thread block per token.  All threads sum the split-K partials
+// (phase 1); warp 0 selects and certifies (phase 2); the experts that level 2
+// must recompute are shared out over the eight warps (phase 3); warp 0
+// finishes the decision, the weights and the blob (phase 4).
 template <int VPL>
 __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ z_part, int S, int T, int D, int E, int k,
@@ -253,46 +257,70 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ wsq_part, float gamma, const __nv_bfloat16* __restrict__ x,
     const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
     int* __restrict__ counters, float gamma2) {
-  extern __shared__ double zx_smem[];  // [8 warps][E] refined logits, then [8][64] uint4 staging
-  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + wib;
+  // shared: zx double[E] (level-3 logits) | sc float2[E] (level-2 pairs) |
+  //         vs float[E] | wss float[E] | clist int[E] | stage uint4[64]
+  extern __shared__ double sel_smem[];
+  double* zx = sel_smem;
+  float2* sc = reinterpret_cast<float2*>(zx + E);
+  float* vs = reinterpret_cast<float*>(sc + E);
+  float* wss = vs + E;
+  int* clist = reinterpret_cast<int*>(wss + E);
+  uint4* stage = reinterpret_cast<uint4*>(sel_smem + (static_cast<size_t>(E) * 28 + 15) / 16 * 2);
+  __shared__ int s_ncand;
+  __shared__ float s_xsq;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x;
   if (t >= T) return;
-  double* zx = zx_smem + static_cast<size_t>(wib) * E;
-  uint4* stage = reinterpret_cast<uint4*>(zx_smem + static_cast<size_t>(8) * E) + wib * 64;
+  const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
 
+  // ---- phase 1: split-K partials of the logits and of the squares, summed in
+  // split order; loads of four splits are issued before their additions.
+  for (int e = tid; e < E; e += blockDim.x) {
+    float a = 0.f, b = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= S; sp += 4) {
+      float z4[4], w4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        z4[q] = __ldg(z_part + (static_cast<size_t>(sp + q) * T + t) * E + e);
+        w4[q] = __ldg(wsq_part + static_cast<size_t>(sp + q) * E + e);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a += z4[q];
+        b += w4[q];
+      }
+    }
+    for (; sp < S; ++sp) {
+      a += __ldg(z_part + (static_cast<size_t>(sp) * T + t) * E + e);
+      b += __ldg(wsq_part + static_cast<size_t>(sp) * E + e);
+    }
+    vs[e] = a;
+    wss[e] = b;
+  }
+  if (tid == 0) {
+    float xs = 0.f;
+    for (int sp = 0; sp < S; ++sp) xs += __ldg(xsq_part + static_cast<size_t>(sp) * T + t);
+    s_xsq = xs;
+    s_ncand = 0;
+  }
+  __syncthreads();
+
+  // ---- phase 2 (warp 0): top-k and certification
   float v[VPL], r[VPL], wn[VPL];
   uint32_t sel = 0, cand = 0;
-  // Split-K partials (logits and sums of squares) summed in split order; the
-  // VPL loads of one split are independent and coalesced across the warp.
-  float xsq = 0.f;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) v[i] = wn[i] = 0.f;
-  for (int sp = 0; sp < S; ++sp) {
-    const float* zp = z_part + (static_cast<size_t>(sp) * T + t) * E;
-    const float* wp = wsq_part + static_cast<size_t>(sp) * E;
-    float part[VPL], sq[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      part[i] = e < E ? __ldg(zp + e) : 0.f;
-      sq[i] = e < E ? __ldg(wp + e) : 0.f;
-    }
-    xsq += __ldg(xsq_part + static_cast<size_t>(sp) * T + t);
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      v[i] += part[i];
-      wn[i] += sq[i];
-    }
-  }
-  const float xn = norm_bound(xsq);
+  int slots = 0;
+  const float xn = norm_bound(s_xsq);
+  if (warp == 0) {
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
-    wn[i] = norm_bound(wn[i]);
     if (e < E) {
-      if (bias) v[i] += __ldg(bias + e);
+      wn[i] = norm_bound(wss[e]);
+      v[i] = vs[e] + (bias ? __ldg(bias + e) : 0.f);
       r[i] = gamma * xn * wn[i] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]);
     } else {
+      wn[i] = 0.f;
       v[i] = -INFINITY;
       r[i] = 0.f;
     }
@@ -351,27 +379,46 @@ __global__ void __launch_bounds__(256) router_select_kernel(
       const bool s_in = (sel >> i) & 1u;
       if ((s_in && v[i] - r[i] <= max_hi) || (!s_in && v[i] + r[i] >= min_lo)) cand |= 1u << i;
     }
-    int slots = __popc(sel & cand);
+    slots = __popc(sel & cand);
 #pragma unroll
     for (int o = 16; o; o >>= 1) slots += __shfl_xor_sync(0xffffffffu, slots, o);
     if (lane == 0 && counters) atomicAdd(counters, 1);
-    const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
-    // Level 2: compensated fp32 logits of every candidate, kept as the
-    // unevaluated pair (s, c) by the lane that owns the expert.
+    // candidate list for phase 3 (ascending i, then lane)
+    int base = 0;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const bool c = (cand >> i) & 1u;
+      const uint32_t bal = __ballot_sync(0xffffffffu, c);
+      if (c) clist[base + __popc(bal & lt_mask)] = lane + 32 * i;
+      base += __popc(bal);
+    }
+    if (lane == 0) s_ncand = base;
+  }
+  }  // warp 0
+  __syncthreads();
+
+  // ---- phase 3 (all warps): level-2 compensated logits of the candidates
+  const int ncand = s_ncand;
+  for (int c = warp; c < ncand; c += blockDim.x / 32) {
+    const int e = clist[c];
+    const float2 z2 = warp_dot_comp(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
+    if (lane == 0) sc[e] = z2;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
+  // ---- phase 4 (warp 0): finish the decision
+  if (ncand > 0) {
     float zs[VPL], zc[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
       zs[i] = zc[i] = 0.f;
-      uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
-      while (bal) {
-        const int src = __ffs(bal) - 1;
-        bal &= bal - 1;
-        const int e = src + 32 * i;
-        const float2 sc = warp_dot_comp(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
-        if (lane == src) {
-          zs[i] = sc.x;
-          zc[i] = sc.y;
-        }
+      if ((cand >> i) & 1u) {
+        const float2 z2 = sc[e];
+        zs[i] = z2.x;
+        zc[i] = z2.y;
       }
     }
     // Values relative to a common reference (the largest candidate sum s):
@@ -534,8 +581,8 @@ cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E
                                  const float* bias, const float* xsq_part, const float* wsq_part,
                                  float gamma, float gamma2, const void* x, const void* wr,
                                  int32_t* blob, int* counters, cudaStream_t st) {
-  const int blocks = (T + 7) / 8;
-  const size_t smem = static_cast<size_t>(8) * E * sizeof(double) + 8 * 64 * sizeof(uint4);
+  const int blocks = T;
+  const size_t smem = (static_cast<size_t>(E) * 28 + 15) / 16 * 16 + 64 * sizeof(uint4);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const auto* wb = static_cast<const __nv_bfloat16*>(wr);
 #define MOE_SELECT_CASE(V)                                                                   \
