@@ -64,7 +64,8 @@ extern "C" {
 
 /* ---- weight formats ---- */
 #define MOE_QUANT_BF16 0    /* bf16 expert weights                                   */
-#define MOE_QUANT_W4A16 1   /* symmetric int4, 8 per int32 (value j in bits 4j..4j+3,
+#define MOE_QUANT_W4A16 1   /* symmetric int4, 8 per int32 in pair order (value 2i
+                               in bits 4i..4i+3, value 2i+1 in bits 16+4i..19+4i,
                                two's complement), bf16 scale per `group` K values [R1] */
 
 /* ---- grouped GEMM operations ---- */

@@ -46,8 +46,9 @@
  *      token index, since a token's ids are distinct).
  *  R6  W_gate_up of an expert is [2I][D]: rows 0..I-1 gate, I..2I-1 up;
  *      W_down is [D][I].  Both are K-major (rows are output features).
- *  R7  int4 packing: 8 values per int32 along K, value j of the 8 in bits
- *      [4j, 4j+4), two's complement.  Scale: one bf16 per (row, group of
+ *  R7  int4 packing: 8 values per int32 along K, in pair order: value 2i of
+ *      the 8 in bits [4i, 4i+4) and value 2i+1 in bits [16+4i, 20+4i)
+ *      (i = 0..3), two's complement.  Scale: one bf16 per (row, group of
  *      `group` consecutive K).  Dequantised weight = q * s, exact in fp64.
  *  R8  Everything after routing is computed in fp64 with no intermediate
  *      rounding.
@@ -75,9 +76,11 @@ static double bf16_to_f64(uint16_t b) {
   return (double)f;
 }
 
-/* Signed value of nibble j (0..7) of a packed int32 word (reading R7). */
+/* Signed value j (0..7) of a packed int32 word (reading R7: value 2i at bit
+ * 4i, value 2i+1 at bit 16+4i). */
 static int nibble_s4(int32_t word, int j) {
-  uint32_t n = (((uint32_t)word) >> (4 * j)) & 0xFu;
+  const int shift = 4 * (j >> 1) + 16 * (j & 1);
+  uint32_t n = (((uint32_t)word) >> shift) & 0xFu;
   return n >= 8 ? (int)n - 16 : (int)n;
 }
 

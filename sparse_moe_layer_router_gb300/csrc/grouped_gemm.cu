@@ -173,27 +173,23 @@ __device__ __forceinline__ int tile_weight_row(const GemmParams& p, const TileIn
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-// Eight signed 4-bit values (value j in bits 4j..4j+3) times a bf16 scale ->
-// eight bf16 in order, each bf16_rne(q * s).  Nibbles become offset binary
-// (q + 8), are placed in the mantissa of 128.0 (0x4300 | u = 128 + u, exact),
-// shifted back by 136 (exact) and multiplied by the scale (one rounding).
+// Eight signed 4-bit values in pair order (value 2i in bits 4i..4i+3, value
+// 2i+1 in bits 16+4i..19+4i) times a bf16 scale -> eight bf16 in order, each
+// bf16_rne(q * s).  One shift and mask put the nibbles of values 2i, 2i+1 in
+// the low bits of the two halves; XOR with 8 makes them offset binary (q + 8)
+// and 0x4300 | u is the bf16 of 128 + u (exact); subtracting 136 (exact) and
+// multiplying by the scale (one rounding) gives the pair, already in order.
 __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
-  const uint32_t x = w ^ 0x88888888u;
   const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
   uint32_t h[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t t = ((x >> (4 * i)) & 0x000F000Fu) | 0x43004300u;  // (e_i, e_{i+4})
+    const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
     __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t), k136);
     __nv_bfloat162 v = __hmul2(q, s2);
     h[i] = *reinterpret_cast<const uint32_t*>(&v);
   }
-  uint4 out;
-  out.x = __byte_perm(h[0], h[1], 0x5410);  // e0, e1
-  out.y = __byte_perm(h[2], h[3], 0x5410);  // e2, e3
-  out.z = __byte_perm(h[0], h[1], 0x7632);  // e4, e5
-  out.w = __byte_perm(h[2], h[3], 0x7632);  // e6, e7
-  return out;
+  return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 // Group table: s.off <- offsets, s.tile_start <- exclusive scan of tiles per
@@ -243,8 +239,9 @@ __device__ __forceinline__ void init_common_barriers(GemmCommon<BN_MAX>& c) {
 }
 
 // Epilogue role (warps 2-5): TMEM accumulators -> h (SwiGLU, bf16) or o
-// (routing-weighted, fp32).
-template <int BN_MAX>
+// (routing-weighted, fp32).  With NP = 2 the accumulator is the sum of two
+// partial accumulators 2 * BN_MAX columns apart (two MMA issuers).
+template <int BN_MAX, int NP = 1>
 __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G, int ntiles,
                               uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
   const int sp = warp & 3;  // TMEM lanes 32*sp .. 32*sp+31
@@ -280,7 +277,16 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
     for (int c0 = 0; c0 < t.bn; c0 += 16) {
       uint32_t r[16];
       tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), r);
-      tmem_wait_ld();
+      if (NP == 2) {
+        uint32_t r2[16];
+        tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(2 * BN_MAX + c0), r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+      } else {
+        tmem_wait_ld();
+      }
       if (p.op == kOpGateUp) {
         // lanes 0-15 hold gate rows, lanes 16-31 the up rows of the same 16
         // features; lane < 16 finishes columns 0-7 of the chunk, lane >= 16
@@ -794,44 +800,75 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 // ==========================================================================
 // W4A16 weights, restored operand in tensor memory (token tiles up to 64 rows)
 // ==========================================================================
-// The eight dequant warps write restored bf16 weight rows straight into TMEM
-// with tcgen05.st (thread = tile row = TMEM lane, two K values per 32-bit
-// column), and the MMA reads A from TMEM.  TMEM holds the double-buffered
-// accumulators (2 x 64 columns) and kTmemABufs operand buffers of 32 columns
-// (one k-block each), so restoring runs up to kTmemABufs k-blocks ahead of the
-// MMA.  Dequant warp w serves TMEM lane quarter w % 4 and the k-blocks j of a
-// packed stage with j % 2 == (w - 6) / 4; k-block index i (running over the
-// CTA's tiles, aligned to packed stages) uses buffer i % kTmemABufs, and since
-// kTmemABufs is a multiple of 4 every buffer is always written by the same
-// four warps.
-constexpr int kTmemABufs = 12;
-constexpr uint32_t kTmemAccCols = 128;  // 2 x 64 accumulator columns
-static_assert(kTmemABufs % kKPerPacked == 0, "buffers must map to fixed warps");
-static_assert(kTmemAccCols + 32 * kTmemABufs <= 512, "TMEM budget");
+// The dequant warps write restored bf16 weight rows straight into TMEM with
+// tcgen05.st (thread = tile row = TMEM lane, two K values per 32-bit column),
+// and the MMA reads A from TMEM, so shared memory carries only the packed
+// weights and the token rows.  Every hand-off is per packed stage (four
+// k-blocks): one packed ring slot, one token ring slot (the token rows of the
+// same four k-blocks) and one TMEM operand slot of 4 x 32 columns.  A
+// tcgen05.mma, a commit and an mbarrier wait each cost tens of cycles on the
+// one issuing thread, and one k-block of int4 weights arrives every ~90 ns at
+// the HBM rate, so the MMA thread waits twice and commits twice per 16 MMAs.
+// Two MMA warps issue in parallel (one issuer alone is bound by its own
+// issue latency): issuer i takes k-blocks 2i, 2i+1 of every packed stage
+// into its own partial accumulator, and the epilogue adds the two.
+// TMEM: 2 issuers x 2 buffers x 64 accumulator columns + kTSlots x 128
+// operand columns = 512.  Dequant warp w serves TMEM lane quarter w % 4 (the
+// quarter a warp may access) and the k-blocks j of each packed stage with
+// j % (ND / 4) == (w - 6) / 4.
+constexpr int kTSlots = 2;
+constexpr int kTIssuers = 2;
+constexpr uint32_t kTmemAccCols = 256;  // 2 issuers x 2 x 64 accumulator columns
+constexpr uint32_t kTSlotCols = 32 * kKPerPacked;
+constexpr int kTokStage = kKPerPacked * 64 * 128;  // token rows of four k-blocks (32 KB)
+static_assert(kTmemAccCols + kTSlotCols * kTSlots <= 512, "TMEM budget");
 
-template <int PSTAGES, int BSTAGES>
+// Token rows of k-block kb in 32-row boxes (the map's box is 32 rows high):
+// ceil(bn / 32) copies; rows past the group (or past the matrix, zero-filled)
+// land in columns the MMA does not read or the epilogue drops.
+__device__ __forceinline__ int tok_boxes32(const TileInfo& t) { return (t.bn + 31) >> 5; }
+__device__ __forceinline__ void load_token_tile32(uint8_t* dst, const CUtensorMap* mb,
+                                                  uint64_t* bar, const TileInfo& t, int kb,
+                                                  uint64_t pol) {
+  for (int i = 0; i < tok_boxes32(t); ++i)
+    tma_load_2d(dst + i * 4096, mb, bar, kb * kBK, t.b_row + 32 * i, pol);
+}
+
+template <int ND>
+__host__ __device__ constexpr int w4t_threads() {
+  return kBaseThreads + 32 * ND + 64;  // + token producer + second MMA issuer
+}
+
+template <int PSTAGES, int TSTAGES>
 struct W4TSmem {
-  uint8_t b[BSTAGES][64 * 128];         // token rows per k-block
+  uint8_t b[TSTAGES][kTokStage];        // token rows, four k-blocks of 64 x 128 B
   uint8_t praw[PSTAGES][kPackedStage];  // packed int4 rows, 128-B swizzle
   uint16_t stab[2][kScaleTabElems];     // group scales of the current tiles
   uint64_t pfull[PSTAGES], pempty[PSTAGES];
-  uint64_t bfull[BSTAGES], bempty[BSTAGES];
-  uint64_t aready[kTmemABufs], afree[kTmemABufs];
+  uint64_t bfull[TSTAGES], bempty[TSTAGES];
+  uint64_t aready[kTSlots], afree[kTSlots];
   uint64_t sfull[2], sempty[2];
+  uint64_t drain2;
   GemmCommon<64> c;
 };
 
-template <int PSTAGES, int BSTAGES>
-__global__ void __launch_bounds__(kW4Threads, 1)
+template <int PSTAGES, int TSTAGES, int ND>
+__global__ void __launch_bounds__(w4t_threads<ND>(), 1)
     grouped_gemm_w4t_kernel(const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_a_s,
                             const __grid_constant__ CUtensorMap tm_b,
                             const __grid_constant__ CUtensorMap tm_b_s,
                             const __grid_constant__ CUtensorMap tm_sc,
                             const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
+  static_assert(ND % 4 == 0 && kKPerPacked % (ND / 4) == 0, "dequant warps per lane quarter");
   constexpr int BN_MAX = 64;
+  constexpr int kThreads = w4t_threads<ND>();
+  constexpr int kTokWarp = 6 + ND;
+  constexpr int kMma2Warp = 7 + ND;
+  constexpr int kSub = ND / 4;                 // dequant warps per TMEM lane quarter
+  constexpr int kMyBlocks = kKPerPacked / kSub;  // k-blocks per packed stage and warp
   extern __shared__ uint8_t smem_raw[];
-  using Smem = W4TSmem<PSTAGES, BSTAGES>;
+  using Smem = W4TSmem<PSTAGES, TSTAGES>;
   const uint32_t raw = smem_u32(smem_raw);
   Smem& s = *reinterpret_cast<Smem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
   GemmCommon<BN_MAX>& cm = s.c;
@@ -844,21 +881,24 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < PSTAGES; ++i) {
       mbar_init(&s.pfull[i], 1);
-      mbar_init(&s.pempty[i], kDequantWarps);
+      mbar_init(&s.pempty[i], ND);
     }
-    for (int i = 0; i < BSTAGES; ++i) {
+    for (int i = 0; i < TSTAGES; ++i) {
       mbar_init(&s.bfull[i], 1);
-      mbar_init(&s.bempty[i], 1);
+      mbar_init(&s.bempty[i], kTIssuers);
     }
-    for (int i = 0; i < kTmemABufs; ++i) {
-      mbar_init(&s.aready[i], 4);  // one warp per TMEM lane quarter
-      mbar_init(&s.afree[i], 1);
+    for (int i = 0; i < kTSlots; ++i) {
+      mbar_init(&s.aready[i], ND);
+      mbar_init(&s.afree[i], kTIssuers);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.sfull[i], 1);
-      mbar_init(&s.sempty[i], kDequantWarps);
+      mbar_init(&s.sempty[i], ND);
     }
     init_common_barriers<BN_MAX>(cm);
+    mbar_init(&cm.tfull[0], kTIssuers);
+    mbar_init(&cm.tfull[1], kTIssuers);
+    mbar_init(&s.drain2, 1);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -871,7 +911,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       if (table) prefetch_tmap(&tm_sc_s);
     }
   }
-  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kW4Threads);
+  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kThreads);
   if (warp == 1) {
     tmem_alloc(&cm.tmem_base, kTmemCols);
     tmem_relinquish();
@@ -883,8 +923,11 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   volatile int* abort_flag = &cm.abort_flag;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane < 4) {
       // ------------------------------------------------ TMA producer: weights + scales
+      // Issuing a tensor copy holds the issuing thread for a few hundred
+      // cycles, so lanes 0-3 issue the four boxes of a gate/up stage side by
+      // side; lane 0 owns the barriers.
       const uint64_t pol_w = policy_evict_first();
       int ps = 0;
       uint32_t pph = 0;
@@ -897,46 +940,52 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         const int row = tile_a_row(p, t);
         if (table) {
           const int sb = tile_ctr & 1;
-          if (!mbar_wait(&s.sempty[sb], ((tile_ctr >> 1) & 1u) ^ 1u, abort_flag)) {
+          bool okw = true;
+          if (lane == 0) okw = mbar_wait(&s.sempty[sb], ((tile_ctr >> 1) & 1u) ^ 1u, abort_flag);
+          if (!__shfl_sync(0xFu, okw, 0)) {
             ok = false;
             break;
           }
           const int ngrp = (t.shared ? p.K_s : p.K) / p.group;
           const CUtensorMap* msc = t.shared ? &tm_sc_s : &tm_sc;
-          mbar_arrive_expect_tx(&s.sfull[sb], static_cast<uint32_t>(kBM * ngrp * 2));
-          if (p.op == kOpGateUp) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&s.sfull[sb], static_cast<uint32_t>(kBM * ngrp * 2));
+            if (p.op == kOpGateUp) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-              tma_load_3d(s.stab[sb] + b * 32 * ngrp, msc, &s.sfull[sb], 0, row + 16 * b, 0,
-                          pol_w);
-          } else {
-            tma_load_2d(s.stab[sb], msc, &s.sfull[sb], 0, row, pol_w);
+              for (int b = 0; b < 4; ++b)
+                tma_load_3d(s.stab[sb] + b * 32 * ngrp, msc, &s.sfull[sb], 0, row + 16 * b, 0,
+                            pol_w);
+            } else {
+              tma_load_2d(s.stab[sb], msc, &s.sfull[sb], 0, row, pol_w);
+            }
           }
           ++tile_ctr;
         }
         for (int kb = 0; kb < t.k_blocks; kb += kKPerPacked) {
-          if (!mbar_wait(&s.pempty[ps], pph ^ 1u, abort_flag)) {
+          bool okw = true;
+          if (lane == 0) okw = mbar_wait(&s.pempty[ps], pph ^ 1u, abort_flag);
+          if (!__shfl_sync(0xFu, okw, 0)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&s.pfull[ps], kPackedStage);
-          p_iss |= 1u << ps;
-          p_issph = (p_issph & ~(1u << ps)) | (pph << ps);
-          const int wc = kb * kBK / 8;
-          if (p.op == kOpGateUp) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-              tma_load_3d(s.praw[ps] + b * 4096, ma, &s.pfull[ps], wc, row + 16 * b, 0, pol_w);
-          } else {
-            tma_load_2d(s.praw[ps], ma, &s.pfull[ps], wc, row, pol_w);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&s.pfull[ps], kPackedStage);
+            p_iss |= 1u << ps;
+            p_issph = (p_issph & ~(1u << ps)) | (pph << ps);
           }
+          __syncwarp(0xFu);
+          const int wc = kb * kBK / 8;
+          if (p.op == kOpGateUp)
+            tma_load_3d(s.praw[ps] + lane * 4096, ma, &s.pfull[ps], wc, row + 16 * lane, 0, pol_w);
+          else if (lane == 0)
+            tma_load_2d(s.praw[ps], ma, &s.pfull[ps], wc, row, pol_w);
           if (++ps == PSTAGES) {
             ps = 0;
             pph ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         record_error(p, abort_flag, MOE_ERR_TIMEOUT);
         for (int i = 0; i < PSTAGES; ++i)
           if ((p_iss >> i) & 1u) mbar_wait_time_only(&s.pfull[i], (p_issph >> i) & 1u);
@@ -946,12 +995,14 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kMma2Warp) {
     if (lane == 0) {
-      // ------------------------------------------------ MMA issuer (A from TMEM)
-      int bs = 0;
-      uint32_t bph = 0;
-      uint32_t idx = 0;
+      // ------------------------------------------------ MMA issuers (A from TMEM)
+      const int is = warp == 1 ? 0 : 1;
+      uint64_t* drain = is == 0 ? &cm.drain : &s.drain2;
+      int ts = 0;
+      uint32_t tph = 0;
+      uint32_t q = 0;  // packed stage counter over the CTA's tiles
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -962,26 +1013,32 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN_MAX);
+        const uint32_t d_tmem =
+            tmem_base + static_cast<uint32_t>(acc * BN_MAX + is * 2 * BN_MAX);
         const uint32_t idesc = idesc_bf16_f32(kBM, t.bn);
-        for (int kb = 0; kb < t.k_blocks; ++kb, ++idx) {
-          const int buf = static_cast<int>(idx % kTmemABufs);
-          if (!mbar_wait(&s.aready[buf], (idx / kTmemABufs) & 1u, abort_flag) ||
-              !mbar_wait(&s.bfull[bs], bph, abort_flag)) {
+        for (int kb0 = 0; kb0 < t.k_blocks; kb0 += kKPerPacked, ++q) {
+          const int slot = static_cast<int>(q % kTSlots);
+          if (!mbar_wait(&s.aready[slot], (q / kTSlots) & 1u, abort_flag) ||
+              !mbar_wait(&s.bfull[ts], tph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem_base + kTmemAccCols + 32u * buf;
-          const uint64_t bd = sdesc_sw128(smem_u32(s.b[bs]));
+          const uint32_t a_slot = tmem_base + kTmemAccCols + kTSlotCols * slot;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ts(d_tmem, a_tmem + 8u * kk, bd + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-          mma_commit(&s.bempty[bs]);
-          mma_commit(&s.afree[buf]);
-          if (++bs == BSTAGES) {
-            bs = 0;
-            bph ^= 1u;
+          for (int jj = 0; jj < kKPerPacked / kTIssuers; ++jj) {
+            const int j = is * (kKPerPacked / kTIssuers) + jj;
+            const uint64_t bd = sdesc_sw128(smem_u32(s.b[ts] + j * (64 * 128)));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_ts(d_tmem, a_slot + 32u * j + 8u * kk, bd + 2u * kk, idesc,
+                          (kb0 | jj | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&s.afree[slot]);
+          mma_commit(&s.bempty[ts]);
+          if (++ts == TSTAGES) {
+            ts = 0;
+            tph ^= 1u;
           }
         }
         if (!ok) break;
@@ -990,52 +1047,60 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
-      mma_commit(&cm.drain);
-      mbar_wait_time_only(&cm.drain, 0);
+      mma_commit(drain);
+      mbar_wait_time_only(drain, 0);
     }
   } else if (warp < 6) {
-    epilogue_role<BN_MAX>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
-  } else if (warp == kTokenWarp) {
-    if (lane == 0) {
+    epilogue_role<BN_MAX, kTIssuers>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
+  } else if (warp == kTokWarp) {
+    if (lane < kKPerPacked) {
       // ------------------------------------------------ TMA producer: token tiles
+      // Lane j issues the token rows of k-block j of the stage; lane 0 owns
+      // the barriers.
       const uint64_t pol_x = policy_evict_last();
-      int bs = 0;
-      uint32_t bph = 0;
+      int ts = 0;
+      uint32_t tph = 0;
       uint32_t b_iss = 0, b_issph = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
         const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
         const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
-        for (int kb = 0; kb < t.k_blocks; ++kb) {
-          if (!mbar_wait(&s.bempty[bs], bph ^ 1u, abort_flag)) {
+        for (int kb0 = 0; kb0 < t.k_blocks; kb0 += kKPerPacked) {
+          bool okw = true;
+          if (lane == 0) okw = mbar_wait(&s.bempty[ts], tph ^ 1u, abort_flag);
+          if (!__shfl_sync(0xFu, okw, 0)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&s.bfull[bs], static_cast<uint32_t>(t.bn) * 128u);
-          b_iss |= 1u << bs;
-          b_issph = (b_issph & ~(1u << bs)) | (bph << bs);
-          load_token_tile(s.b[bs], mb, &s.bfull[bs], t, kb, pol_x);
-          if (++bs == BSTAGES) {
-            bs = 0;
-            bph ^= 1u;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&s.bfull[ts],
+                                  static_cast<uint32_t>(tok_boxes32(t)) * 4096u * kKPerPacked);
+            b_iss |= 1u << ts;
+            b_issph = (b_issph & ~(1u << ts)) | (tph << ts);
+          }
+          __syncwarp(0xFu);
+          load_token_tile32(s.b[ts] + lane * (64 * 128), mb, &s.bfull[ts], t, kb0 + lane, pol_x);
+          if (++ts == TSTAGES) {
+            ts = 0;
+            tph ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         record_error(p, abort_flag, MOE_ERR_TIMEOUT);
-        for (int i = 0; i < BSTAGES; ++i)
+        for (int i = 0; i < TSTAGES; ++i)
           if ((b_iss >> i) & 1u) mbar_wait_time_only(&s.bfull[i], (b_issph >> i) & 1u);
       }
     }
-  } else {
+  } else if (warp < kTokWarp) {
     // -------------------------------------------------- dequant warps -> TMEM
     const int qd = warp & 3;                 // TMEM lane quarter
-    const int hd = (warp - 6) / 4;           // k-blocks j with j % 2 == hd
+    const int hd = (warp - 6) / 4;           // k-blocks j with j % kSub == hd
     const int r = 32 * qd + lane;            // tile row == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
     int ps = 0;
     uint32_t pph = 0;
-    uint32_t idx = 0;  // running k-block index, aligned to packed stages
+    uint32_t q = 0;
     uint32_t tile_ctr = 0;
     bool ok = true;
     for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
@@ -1049,52 +1114,59 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         ok = false;
         break;
       }
-      for (int kb0 = 0; kb0 < t.k_blocks && ok; kb0 += kKPerPacked, idx += kKPerPacked) {
+      for (int kb0 = 0; kb0 < t.k_blocks; kb0 += kKPerPacked, ++q) {
         if (!mbar_wait(&s.pfull[ps], pph, abort_flag)) {
           ok = false;
           break;
         }
+        // This warp's packed words leave shared memory first, so the packed
+        // slot is released before the (longer) restore.
         const uint8_t* prow = s.praw[ps] + r * 128;
+        uint4 pk[kMyBlocks][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int j = 2 * h + hd;  // k-block within the packed stage
-          const uint32_t i = idx + j;
-          const int buf = static_cast<int>(i % kTmemABufs);
-          const int g = ((kb0 + j) * kBK) / p.group;
-          const uint16_t sbits = table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
-          __nv_bfloat162 s2;
-          s2.x = __ushort_as_bfloat16(sbits);
-          s2.y = s2.x;
-          const uint4 p0 = *reinterpret_cast<const uint4*>(prow + (((2 * j) ^ (r & 7)) << 4));
-          const uint4 p1 = *reinterpret_cast<const uint4*>(prow + (((2 * j + 1) ^ (r & 7)) << 4));
-          const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          uint32_t v[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 q = dequant_word(words[c], s2);
-            v[4 * c] = q.x;
-            v[4 * c + 1] = q.y;
-            v[4 * c + 2] = q.z;
-            v[4 * c + 3] = q.w;
-          }
-          if (!mbar_wait(&s.afree[buf], ((i / kTmemABufs) & 1u) ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          tmem_st_32x32b_x32(tmem_base + lane_addr + kTmemAccCols + 32u * buf, v);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s.aready[buf]);
+        for (int h = 0; h < kMyBlocks; ++h) {
+          const int j = kSub * h + hd;
+          pk[h][0] = *reinterpret_cast<const uint4*>(prow + (((2 * j) ^ (r & 7)) << 4));
+          pk[h][1] = *reinterpret_cast<const uint4*>(prow + (((2 * j + 1) ^ (r & 7)) << 4));
         }
-        if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.pempty[ps]);
         if (++ps == PSTAGES) {
           ps = 0;
           pph ^= 1u;
         }
+        const int slot = static_cast<int>(q % kTSlots);
+        if (!mbar_wait(&s.afree[slot], ((q / kTSlots) & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_slot = tmem_base + lane_addr + kTmemAccCols + kTSlotCols * slot;
+#pragma unroll
+        for (int h = 0; h < kMyBlocks; ++h) {
+          const int j = kSub * h + hd;
+          const int g = ((kb0 + j) * kBK) / p.group;
+          const uint16_t sbits = table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
+          __nv_bfloat162 s2;
+          s2.x = __ushort_as_bfloat16(sbits);
+          s2.y = s2.x;
+          const uint32_t words[8] = {pk[h][0].x, pk[h][0].y, pk[h][0].z, pk[h][0].w,
+                                     pk[h][1].x, pk[h][1].y, pk[h][1].z, pk[h][1].w};
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 d = dequant_word(words[c], s2);
+            v[4 * c] = d.x;
+            v[4 * c + 1] = d.y;
+            v[4 * c + 2] = d.z;
+            v[4 * c + 3] = d.w;
+          }
+          tmem_st_32x32b_x32(a_slot + 32u * j, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.aready[slot]);
       }
       if (!ok) break;
       if (table) {
@@ -1138,15 +1210,15 @@ static cudaError_t launch_w4(const GemmParams& p, const GemmMaps& m, int num_sms
   return cudaGetLastError();
 }
 
-template <int PSTAGES, int BSTAGES>
+template <int PSTAGES, int TSTAGES, int ND>
 static cudaError_t launch_w4t(const GemmParams& p, const GemmMaps& m, int num_sms,
                               cudaStream_t st) {
-  const size_t smem = sizeof(W4TSmem<PSTAGES, BSTAGES>) + 1024;
-  auto kern = grouped_gemm_w4t_kernel<PSTAGES, BSTAGES>;
+  const size_t smem = sizeof(W4TSmem<PSTAGES, TSTAGES>) + 1024;
+  auto kern = grouped_gemm_w4t_kernel<PSTAGES, TSTAGES, ND>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kW4Threads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
+  kern<<<num_sms, w4t_threads<ND>(), smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
   return cudaGetLastError();
 }
 
@@ -1156,7 +1228,7 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int b
     if (bn_max == 64) return launch_bf16<64, 8>(p, maps, num_sms, st);
     if (bn_max == 256) return launch_bf16<256, 4>(p, maps, num_sms, st);
   } else if (quant == 1) {
-    if (bn_max == 64) return launch_w4t<4, 12>(p, maps, num_sms, st);
+    if (bn_max == 64) return launch_w4t<6, 3, 16>(p, maps, num_sms, st);
     if (bn_max == 256) return launch_w4<256, 3, 2>(p, maps, num_sms, st);
   }
   return cudaErrorInvalidValue;

@@ -347,6 +347,9 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   p.K = gate_up ? c->D : c->I;
   p.K_s = gate_up ? c->D : c->I_shared;
   p.group = w4 ? c->group : 128;
+  const int bn_max = choose_bn_max(c);
+  // The W4A16 64-row kernel copies token rows in 32-row boxes, the others in 16.
+  const uint32_t tok_rows = (w4 && bn_max == 64) ? 32 : 16;
   bool ok = true;
   if (gate_up) {
     p.m_tiles = c->I / 64;
@@ -357,11 +360,11 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     p.ld_out_s = c->I_shared;
     ok &= w4 ? map_gate_up_i4(&maps.a, a->w, c->E, c->I, c->D)
              : map_gate_up_bf16(&maps.a, a->w, c->E, c->I, c->D);
-    ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, 16);
+    ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, tok_rows);
     if (has_shared) {
       ok &= w4 ? map_gate_up_i4(&maps.a_s, a->w_shared, 1, c->I_shared, c->D)
                : map_gate_up_bf16(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
-      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->D, 16);
+      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->D, tok_rows);
     }
   } else {
     p.m_tiles = c->D / 128;
@@ -373,16 +376,15 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     p.ld_out_s = c->D;
     ok &= w4 ? map_2d_i4(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128)
              : map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128);
-    ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, 16);
+    ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, tok_rows);
     if (has_shared) {
       ok &= w4 ? map_2d_i4(&maps.a_s, a->w_shared, c->D, c->I_shared, 128)
                : map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
-      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, 16);
+      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, tok_rows);
     }
   }
   // W4A16 scale tables by TMA when every K of the launch is a multiple of 1024
   // up to 4096 (whole rows of 8..32 scales, 16..64 B) and the 64-row variant runs.
-  const int bn_max = choose_bn_max(c);
   const bool k_ok = p.K % 1024 == 0 && p.K <= 4096 && (!has_shared || (p.K_s % 1024 == 0 &&
                                                                       p.K_s <= 4096));
   p.scale_table = (w4 && bn_max == 64 && k_ok) ? 1 : 0;

@@ -16,7 +16,7 @@ so that about a fifth of the experts receive no token.
 
 The W4A16 configuration quantises the same bf16 weights to symmetric int4
 (range -8..7, no zero point), group 128 along K, bf16 scale per group, packed
-8 values per int32 with value j in bits [4j, 4j+4).
+8 values per int32 in pair order (value 2i at bit 4i, value 2i+1 at bit 16+4i).
 """
 from __future__ import annotations
 
@@ -97,12 +97,17 @@ def zipf_bias(E: int, s: float, alpha: float, seed: int) -> torch.Tensor:
     return (alpha * logp).to(torch.float32)
 
 
+# Bit position of value j (0..7) of a packed int32: pairs (2i, 2i+1) at bits 4i and 16+4i.
+PACK_SHIFTS = (0, 16, 4, 20, 8, 24, 12, 28)
+
+
 def quantize_w4(w: torch.Tensor, group: int = 128):
     """Symmetric int4, one bf16 scale per ``group`` consecutive K values.
 
     w: [..., R, C] bf16.  Returns (q [..., R, C/8] int32, s [..., R, C/group] bf16)
     with s = bf16(absmax / 7), q = clamp(round_half_even(w / s), -8, 7) (q = 0
-    where s = 0), and value j of each group of 8 in bits [4j, 4j+4).
+    where s = 0).  Pair order within each int32: value 2i of the group of 8 in
+    bits [4i, 4i+4), value 2i+1 in bits [16+4i, 20+4i).
     """
     *lead, R, C = w.shape
     assert C % group == 0 and C % 8 == 0
@@ -113,7 +118,7 @@ def quantize_w4(w: torch.Tensor, group: int = 128):
     q = torch.round(wf / safe).clamp_(-8, 7)
     q = torch.where(sf == 0, torch.zeros_like(q), q).to(torch.int32)
     q = q.reshape(*lead, R, C // 8, 8) & 0xF
-    shifts = torch.arange(0, 32, 4, device=w.device, dtype=torch.int32)
+    shifts = torch.tensor(PACK_SHIFTS, device=w.device, dtype=torch.int32)
     packed = torch.zeros((*lead, R, C // 8), dtype=torch.int64, device=w.device)
     packed = (q.to(torch.int64) << shifts.to(torch.int64)).sum(dim=-1)
     packed = torch.where(packed >= 2**31, packed - 2**32, packed).to(torch.int32)

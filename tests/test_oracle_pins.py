@@ -332,16 +332,26 @@ def test_forward_hand_closed_form():
 
 # ---------------------------------------------------------------- W4A16
 def pack_by_hand(q):
-    """Pack a [R, C] array of ints in [-8, 7] with Python integers, value j of 8 in bits 4j."""
+    """Pack a [R, C] array of ints in [-8, 7] with Python integers, pair order: value 2i
+    of each 8 in bits 4i, value 2i+1 in bits 16+4i."""
     R, C = q.shape
     out = np.zeros((R, C // 8), np.int64)
     for r in range(R):
         for c8 in range(C // 8):
             word = 0
             for j in range(8):
-                word |= (int(q[r, c8 * 8 + j]) & 0xF) << (4 * j)
+                word |= (int(q[r, c8 * 8 + j]) & 0xF) << (4 * (j // 2) + 16 * (j % 2))
             out[r, c8] = word - (1 << 32) if word >= (1 << 31) else word
     return out.astype(np.int32)
+
+
+def test_dequant_w4_literal_word():
+    """0x86427531 holds, in pair order, the values 1..7 and -8: nibbles from bit 0 up are
+    1 3 5 7 (values 0, 2, 4, 6) and 2 4 6 8 (values 1, 3, 5, 7; 0x8 is -8)."""
+    word = np.array([[0x86427531 - (1 << 32)]], np.int32)
+    s = bf16_bits(np.array([[0.5]]))
+    out = oracle.dequant_w4(word, s, 8)
+    assert out.tolist() == [[0.5, 1.0, 1.5, 2.0, 2.5, 3.0, 3.5, -4.0]]
 
 
 def test_dequant_w4_nibble_order_sign_and_scales():
