@@ -110,6 +110,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "l"(policy)
+      : "memory");
+}
+
 // Waits with only the time bound (used while unwinding after an abort).
 __device__ __forceinline__ bool mbar_wait_time_only(uint64_t* bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
@@ -331,6 +341,17 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
   }
 }
 
+// Token tile of k-block kb with 32-row boxes (mb32) and, for a remainder of
+// 16 rows, one 16-row box (mb16): issuing a copy holds the issuing thread for
+// a few hundred cycles, so a tile takes as few copies as its rows allow.
+__device__ __forceinline__ void load_token_tile2(uint8_t* dst, const CUtensorMap* mb16,
+                                                 const CUtensorMap* mb32, uint64_t* bar,
+                                                 const TileInfo& t, int kb, uint64_t pol) {
+  int i = 0;
+  for (; i + 32 <= t.bn; i += 32) tma_load_2d(dst + i * 128, mb32, bar, kb * kBK, t.b_row + i, pol);
+  if (i < t.bn) tma_load_2d(dst + i * 128, mb16, bar, kb * kBK, t.b_row + i, pol);
+}
+
 // Token tile of k-block kb: bn rows of 64 K in 16-row boxes (128-B swizzle).
 __device__ __forceinline__ void load_token_tile(uint8_t* dst, const CUtensorMap* mb, uint64_t* bar,
                                                 const TileInfo& t, int kb, uint64_t pol) {
@@ -346,7 +367,9 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_a_s,
                         const __grid_constant__ CUtensorMap tm_b,
-                        const __grid_constant__ CUtensorMap tm_b_s, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tm_b_s,
+                        const __grid_constant__ CUtensorMap tm_b2,
+                        const __grid_constant__ CUtensorMap tm_b2_s, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = Bf16Smem<BN_MAX, STAGES>;
   const uint32_t raw = smem_u32(smem_raw);
@@ -368,9 +391,11 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
   if (threadIdx.x == 32) {
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
+    prefetch_tmap(&tm_b2);
     if (p.has_shared) {
       prefetch_tmap(&tm_a_s);
       prefetch_tmap(&tm_b_s);
+      prefetch_tmap(&tm_b2_s);
     }
   }
   const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kBaseThreads);
@@ -398,6 +423,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
         const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
         const CUtensorMap* ma = t.shared ? &tm_a_s : &tm_a;
         const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
+        const CUtensorMap* mb2 = t.shared ? &tm_b2_s : &tm_b2;
         const uint32_t bytes = kAStage + static_cast<uint32_t>(t.bn) * 128u;
         const int row = tile_a_row(p, t);
         for (int kb = 0; kb < t.k_blocks; ++kb) {
@@ -408,15 +434,11 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
           mbar_arrive_expect_tx(&s.full[stage], bytes);
           issued |= 1u << stage;
           issued_ph = (issued_ph & ~(1u << stage)) | (phase << stage);
-          if (p.op == kOpGateUp) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-              tma_load_3d(s.a[stage] + b * 4096, ma, &s.full[stage], kb * kBK, row + 16 * b, 0,
-                          pol_w);
-          } else {
+          if (p.op == kOpGateUp)
+            tma_load_4d(s.a[stage], ma, &s.full[stage], kb * kBK, 0, 0, row / 16, pol_w);
+          else
             tma_load_2d(s.a[stage], ma, &s.full[stage], kb * kBK, row, pol_w);
-          }
-          load_token_tile(s.b[stage], mb, &s.full[stage], t, kb, pol_x);
+          load_token_tile2(s.b[stage], mb, mb2, &s.full[stage], t, kb, pol_x);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -1194,7 +1216,7 @@ static cudaError_t launch_bf16(const GemmParams& p, const GemmMaps& m, int num_s
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kBaseThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, p);
+  kern<<<num_sms, kBaseThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.b2, m.b2_s, p);
   return cudaGetLastError();
 }
 

@@ -107,6 +107,24 @@ bool map_gate_up_bf16(CUtensorMap* m, const void* base, uint64_t groups, uint64_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Gate/up weights [groups][2*half][cols] bf16 as a 4-D map {64-element K
+// chunk, 16 rows, gate/up, 16-row block}: one {64, 16, 2, 4} box is a whole
+// 64-feature k-block stage (four blocks of 16 gate rows followed by their 16
+// up rows, 16 KB), one copy where the 3-D map takes four.
+bool map_gate_up_bf16_4d(CUtensorMap* m, const void* base, uint64_t groups, uint64_t half,
+                         uint64_t cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const uint64_t rb = cols * 2;  // bytes per row
+  const cuuint64_t dims[4] = {cols, 16, 2, groups * 2 * half / 16};
+  const cuuint64_t strides[3] = {rb, half * rb, 16 * rb};
+  const cuuint32_t box[4] = {64, 16, 2, 4};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Packed int4 weights [rows][cols/8] int32: 2-D map with a {32 words = 256
 // values = 128 B, box_rows} box and the 128-byte swizzle.
 bool map_2d_i4(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
@@ -359,12 +377,14 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     p.ld_out = c->I;
     p.ld_out_s = c->I_shared;
     ok &= w4 ? map_gate_up_i4(&maps.a, a->w, c->E, c->I, c->D)
-             : map_gate_up_bf16(&maps.a, a->w, c->E, c->I, c->D);
+             : map_gate_up_bf16_4d(&maps.a, a->w, c->E, c->I, c->D);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, tok_rows);
+    if (!w4) ok &= map_2d_bf16(&maps.b2, b_routed, P, c->D, 32);
     if (has_shared) {
       ok &= w4 ? map_gate_up_i4(&maps.a_s, a->w_shared, 1, c->I_shared, c->D)
-               : map_gate_up_bf16(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
+               : map_gate_up_bf16_4d(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->D, tok_rows);
+      if (!w4) ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->D, 32);
     }
   } else {
     p.m_tiles = c->D / 128;
@@ -377,10 +397,12 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     ok &= w4 ? map_2d_i4(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128)
              : map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, tok_rows);
+    if (!w4) ok &= map_2d_bf16(&maps.b2, b_routed, P, c->I, 32);
     if (has_shared) {
       ok &= w4 ? map_2d_i4(&maps.a_s, a->w_shared, c->D, c->I_shared, 128)
                : map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, tok_rows);
+      if (!w4) ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->I_shared, 32);
     }
   }
   // W4A16 scale tables by TMA when every K of the launch is a multiple of 1024
@@ -397,10 +419,12 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     }
   }
   if (!ok) return MOE_ERR_CUDA;
+  if (w4) maps.b2 = maps.b;
   if (!has_shared) {
     maps.a_s = maps.a;
     maps.b_s = maps.b;
   }
+  if (w4 || !has_shared) maps.b2_s = maps.b_s;
   if (!p.scale_table || !has_shared) maps.sc_s = maps.a_s;
   if (!p.scale_table) maps.sc = maps.a;
   return cuda_rc(launch_grouped_gemm(p, maps, bn_max, c->quant, dev.sms, st));

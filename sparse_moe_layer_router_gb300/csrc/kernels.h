@@ -71,6 +71,7 @@ struct GemmParams {
 struct GemmMaps {
   CUtensorMap a, a_s, b, b_s;  // weights (routed, shared), activations (routed, shared)
   CUtensorMap sc, sc_s;        // W4A16 group scales (routed, shared)
+  CUtensorMap b2, b2_s;        // bf16 kernels: activations in 32-row boxes (b, b_s: 16 rows)
 };
 
 // Kernel variants: BN_MAX token rows per tile (64 or 256); quant 0 = bf16, 1 = W4A16.
