@@ -157,13 +157,29 @@ size_t moe_workspace_size(const moe_config *cfg, int entry);
  *   blob int32 [T][2][k]: blob[t][0][j] = expert id (ascending in j),
  *                         blob[t][1][j] = fp32 bit pattern of its weight.
  * The selected set equals the one decided by fp64 index-order logits: fp32
- * logits carry a rigorous error radius, and tokens whose boundary is not
- * certified are re-decided in fp64.
+ * tensor-core logits carry an error radius, and tokens whose boundary it does
+ * not certify are re-decided with a compensated fp32 sum and, if still not
+ * separated, with the fp64 definition itself.
  *   x bf16 [T][D], w_router bf16 [E][D], bias fp32 [E] or NULL.
  */
 int moe_route(const moe_config *cfg, const void *x, const void *w_router,
               const float *bias, int32_t *blob, void *ws, size_t ws_bytes,
               void *stream);
+
+/*
+ * Router logits [P1] ("Systems engineering playbook: optimizing Qwen 3.5-397B
+ * MoE on Ironwood (TPU7x)", section 1: the router gate projection), the first
+ * step of moe_route on its own:
+ *   z fp32 [T][E] = x.Wr^T (no bias), computed on the tensor cores with one
+ *   fresh fp32 accumulator per 64-wide K chunk and the chunk values added in
+ *   K order.  moe_route certifies its decisions assuming
+ *   |z - exact| <= 2^-15 * sum_d |x_d Wr_ed| + (D/64 + 2) * 2^-24 * sum_d |x_d Wr_ed|.
+ *   x bf16 [T][D], w_router bf16 [E][D]; ws sized for MOE_ENTRY_ROUTE.
+ * Errors: as moe_route; a device wait that runs out sets MOE_ERR_TIMEOUT in
+ * the status word (moe_get_status).
+ */
+int moe_router_logits(const moe_config *cfg, const void *x, const void *w_router, float *z,
+                      void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Dispatch [P3B]: group the T*k (token, slot) pairs by expert, stable in the

@@ -36,7 +36,7 @@ MOE_ENTRY_FORWARD = 3
 MOE_ENTRY_FORWARD_HOST = 4
 
 # Every function declared in include/moe.h.
-EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_static",
+EXPORTS = ("moe_workspace_size", "moe_route", "moe_router_logits", "moe_permute", "moe_permute_static",
            "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status",
            "moe_selftest_wait_timeout", "moe_strerror")
 
@@ -83,6 +83,7 @@ def lib():
             L.moe_workspace_size.argtypes = [cfgp, I]
             L.moe_workspace_size.restype = S
             L.moe_route.argtypes = [cfgp, P, P, P, P, P, S, P]
+            L.moe_router_logits.argtypes = [cfgp, P, P, P, P, S, P]
             L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, P, P, S, P]
             L.moe_permute_static.argtypes = [cfgp, P, P, P, P, P, P, P, P]
             L.moe_grouped_gemm.argtypes = [cfgp, ctypes.POINTER(MoeGemmArgs), P, S, P]
@@ -93,7 +94,7 @@ def lib():
             L.moe_selftest_wait_timeout.argtypes = [P, S, ctypes.c_uint, P]
             L.moe_strerror.argtypes = [I]
             L.moe_strerror.restype = ctypes.c_char_p
-            for n in ("moe_route", "moe_permute", "moe_permute_static", "moe_grouped_gemm",
+            for n in ("moe_route", "moe_router_logits", "moe_permute", "moe_permute_static", "moe_grouped_gemm",
                       "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status",
                       "moe_selftest_wait_timeout"):
                 getattr(L, n).restype = I
@@ -154,6 +155,17 @@ def route(cfg, x, w_router, bias=None, blob=None, ws=None, stream=None):
     _check(lib().moe_route(ctypes.byref(config(cfg)), _p(x), _p(w_router), _p(bias), _p(blob),
                            _p(ws), ws.numel(), _stream(stream)), "moe_route")
     return blob
+
+
+def router_logits(cfg, x, w_router, z=None, ws=None, stream=None):
+    """fp32 [T, E] level-1 router logits x . Wr^T (tensor cores, no bias)."""
+    if z is None:
+        z = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(cfg, MOE_ENTRY_ROUTE, x.device)
+    _check(lib().moe_router_logits(ctypes.byref(config(cfg)), _p(x), _p(w_router), _p(z), _p(ws),
+                                   ws.numel(), _stream(stream)), "moe_router_logits")
+    return z
 
 
 def permute(cfg, blob, ws=None, stream=None, x=None, x_perm=None, out=None):

@@ -70,6 +70,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Waits with only the time bound (used while unwinding after an abort).
+__device__ __forceinline__ bool mbar_wait_time_only_r(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -173,6 +182,12 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+// Ties registers written by tcgen05.ld to a point after tcgen05.wait::ld, so
+// no use of them can be scheduled between the load and the wait.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

@@ -202,21 +202,23 @@ int validate(const moe_config* c) {
 }
 
 // ---------------------------------------------------------------- workspace
+// Router logits on the tensor cores: CTAs of 128 experts x 64 tokens, split
+// over K (k-blocks of 64) until about kRouterTargetCtas CTAs run.
 struct RouterPlan {
   int S = 1;
-  int sub_per_split = 1;
+  int kb_per_split = 1;
 };
 
 RouterPlan router_plan(const moe_config* c) {
   RouterPlan r;
-  const int nsub = c->D / 64;
-  const long base = static_cast<long>((c->E + 63) / 64) * ((c->T + 63) / 64);
+  const int nkb = c->D / 64;
+  const long base = static_cast<long>((c->E + 127) / 128) * ((c->T + 63) / 64);
   long S = (kRouterTargetCtas + base - 1) / base;
   if (S > 16) S = 16;
-  if (S > nsub) S = nsub;
+  if (S > nkb) S = nkb;
   if (S < 1) S = 1;
-  r.sub_per_split = (nsub + static_cast<int>(S) - 1) / static_cast<int>(S);
-  r.S = (nsub + r.sub_per_split - 1) / r.sub_per_split;
+  r.kb_per_split = (nkb + static_cast<int>(S) - 1) / static_cast<int>(S);
+  r.S = (nkb + r.kb_per_split - 1) / r.kb_per_split;
   return r;
 }
 
@@ -246,8 +248,8 @@ Layout layout(const moe_config* c, int entry) {
   const size_t chunks = (P + kPermuteChunk - 1) / kPermuteChunk;
   auto route_part = [&] {
     L.zpart = cv.take(static_cast<size_t>(rp.S) * T * E * 4);
-    L.xnorm = cv.take(static_cast<size_t>(rp.S) * T * 4);  // split partial sums of squares
-    L.wnorm = cv.take(static_cast<size_t>(rp.S) * E * 4);
+    L.xnorm = cv.take(T * 4);  // sums of squares of the token rows
+    L.wnorm = cv.take(E * 4);  // and of the router rows
   };
   switch (entry) {
     case MOE_ENTRY_ROUTE:
@@ -292,14 +294,16 @@ T* at(void* ws, size_t off) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Error radius factor of the fp32 router logits (see router.cu): products pass
-// through at most h = 64 + sub_per_split + S + 2 fp32 roundings; the fp64
-// index-order definition deviates from the exact sum by at most D * 2^-53
-// relative to sum |x_d w_d|.
+// Error radius factor of the tensor-core router logits (see router.cu): at
+// most 2^-15 of sum|x w| from each 64-wide chunk's accumulation, then every
+// chunk value passes through at most h = kb_per_split + S + 2 fp32 roundings
+// (running sum, split sum, bias); the fp64 index-order definition deviates from
+// the exact sum by at most D * 2^-53 relative to sum |x_d w_d|.
 float router_gamma(const moe_config* c, const RouterPlan& rp) {
   const double u = std::ldexp(1.0, -24);
-  const double h = 64.0 + rp.sub_per_split + rp.S + 2.0;
-  const double g = h * u / (1.0 - h * u) + c->D * std::ldexp(1.0, -53) * 1.01;
+  const double h = rp.kb_per_split + rp.S + 2.0;
+  const double g = std::ldexp(1.0, -15) * (1.0 + std::ldexp(1.0, -10)) + h * u / (1.0 - h * u) +
+                   c->D * std::ldexp(1.0, -53) * 1.01;
   return std::nextafter(static_cast<float>(g), INFINITY);
 }
 
@@ -323,7 +327,13 @@ int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* w
   float* zpart = at<float>(ws, L.zpart);
   float* xsq = at<float>(ws, L.xnorm);
   float* wsq = at<float>(ws, L.wnorm);
-  launch_router_logits(x, wr, c->T, c->D, c->E, rp.S, rp.sub_per_split, zpart, xsq, wsq, st);
+  CUtensorMap mw, mx;
+  if (!map_2d_bf16(&mw, wr, c->E, c->D, 128) || !map_2d_bf16(&mx, x, c->T, c->D, 64))
+    return MOE_ERR_CUDA;
+  const int rc = cuda_rc(launch_router_logits_tc(mw, mx, x, wr, c->T, c->D, c->E, rp.S,
+                                                 rp.kb_per_split, zpart, xsq, wsq,
+                                                 at<int>(ws, 0), st));
+  if (rc != MOE_OK) return rc;
   return cuda_rc(launch_router_select(zpart, rp.S, c->T, c->D, c->E, c->k, bias, xsq, wsq,
                                       router_gamma(c, rp), router_gamma2(c), x, wr, blob,
                                       at<int>(ws, 4), st));
@@ -533,6 +543,25 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_router, const 
   int rc = begin(cfg, MOE_ENTRY_ROUTE, ws, ws_bytes, &dev, &L);
   if (rc) return rc;
   return route_impl(cfg, dev, x, w_router, bias, blob, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+int moe_router_logits(const moe_config* cfg, const void* x, const void* w_router, float* z,
+                      void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !w_router || !z) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(z)) return MOE_ERR_ALIGN;
+  DevInfo dev;
+  Layout L;
+  int rc = begin(cfg, MOE_ENTRY_ROUTE, ws, ws_bytes, &dev, &L);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 12, st) != cudaSuccess) return MOE_ERR_CUDA;
+  CUtensorMap mw, mx;
+  if (!map_2d_bf16(&mw, w_router, cfg->E, cfg->D, 128) || !map_2d_bf16(&mx, x, cfg->T, cfg->D, 64))
+    return MOE_ERR_CUDA;
+  // one split: z itself is the split's output
+  return cuda_rc(launch_router_logits_tc(mw, mx, x, w_router, cfg->T, cfg->D, cfg->E, 1,
+                                         cfg->D / 64, z, at<float>(ws, L.xnorm),
+                                         at<float>(ws, L.wnorm), at<int>(ws, 0), st));
 }
 
 int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int32_t* offsets,

@@ -10,9 +10,10 @@ namespace moe {
 constexpr int kPermuteChunk = 2048;  // pairs per permute block
 
 // ---- router (router.cu)
-void launch_router_logits(const void* x, const void* wr, int T, int D, int E, int S,
-                          int sub_per_split, float* z_part, float* xsq_part, float* wsq_part,
-                          cudaStream_t st);
+cudaError_t launch_router_logits_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                                    const void* x, const void* wr, int T, int D, int E, int S,
+                                    int kbs, float* z_part, float* xsq, float* wsq, int* status,
+                                    cudaStream_t st);
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
                                  const float* bias, const float* xsq_part, const float* wsq_part,
                                  float gamma, float gamma2, const void* x, const void* wr,

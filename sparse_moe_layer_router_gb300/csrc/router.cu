@@ -9,10 +9,11 @@
 //
 // Routing decision.  The deciding logit is defined as the fp64 sum, in index
 // order, of the exact products x[t,d]*Wr[e,d] (plus the fp32 bias, added
-// last).  The GPU computes fp32 logits v with a summation tree of bounded
-// depth h, so |v - z| <= r = gamma_h * ||x_t|| * ||Wr_e|| + 2^-23 |v| (the
-// Cauchy-Schwarz bound on sum |x_d Wr_ed|, plus the fp64 definition's own
-// deviation folded into gamma).  A token whose k-th / (k+1)-th boundary is
+// last).  The GPU computes fp32 logits v on the tensor cores, one fresh
+// accumulator per 64-wide K chunk whose fp32 values are then added in order,
+// so |v - z| <= r = gamma * ||x_t|| * ||Wr_e|| + 2^-23 |v| (the Cauchy-Schwarz
+// bound on sum |x_d Wr_ed|; gamma covers the chunk accumulation, the chunk and
+// split sums and the fp64 definition's own deviation).  A token whose k-th / (k+1)-th boundary is
 // separated by these intervals is certified; otherwise the experts whose
 // intervals straddle the boundary are recomputed with a compensated fp32 dot
 // product whose rigorous radius is ~1e-10 of sum |x_d w_d| (level 2), and only
@@ -24,114 +25,197 @@
 
 namespace moe {
 
-// ---------------------------------------------------------------- logits
-// z_part[split][t][e] = sum over the split's K range of x[t,k] * Wr[e,k] (fp32).
-// Within the range, products are accumulated in sub-chunks of 64 (a fresh fp32
-// accumulator each) and sub-chunk sums are added to the running total, so each
-// product passes through at most 64 + sub_per_split roundings.
-// The same pass also produces partial sums of squares of the x rows (CTAs with
-// blockIdx.x == 0) and of the router rows (blockIdx.y == 0) for the error
-// radius; every element is squared once per split.
-// Global loads of chunk c+1 are issued before chunk c is multiplied (register
-// staging, two shared-memory buffers, one barrier per 32-wide chunk).
-constexpr int kRT = 64, kRE = 64, kRK = 32;
+// ---------------------------------------------------------------- logits (tensor cores)
+// z_part[split][t][e] = sum over the split's k-blocks of x[t, kb] . Wr[e, kb]
+// (64-wide K chunks).  A CTA computes 128 experts (MMA M, TMEM lanes) x 64
+// tokens (MMA N) for one split: every k-block is four chained bf16 MMAs into a
+// fresh fp32 accumulator (one of two TMEM buffers), which the four epilogue
+// warps read and add, in k-block order, to running fp32 sums in registers.
+// The tensor core's fp32 accumulation order and rounding are not documented;
+// the error radius assumes at most 2^-15 * sum|x w| over each 64-wide chunk
+// (about four times the bound of an accumulation that aligns the terms to the
+// largest one and truncates to 24 bits), and a GPU test checks the measured
+// error against a bound twice as tight.  Warp 0: TMA producer; warp 1:
+// TMEM allocation and MMA issue; warps 2-5: epilogue.
+constexpr int kRtE = 128, kRtT = 64, kRtStages = 4;
 
-__global__ void __launch_bounds__(256) router_logits_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wr, int T, int D,
-    int E, int sub_per_split, float* __restrict__ z_part, float* __restrict__ xsq_part,
-    float* __restrict__ wsq_part) {
-  __shared__ __align__(16) float xs[2][kRK][kRT + 4];
-  __shared__ __align__(16) float ws[2][kRK][kRE + 4];
-  const int e0 = blockIdx.x * kRE, t0 = blockIdx.y * kRT, split = blockIdx.z;
-  const int nsub = D / 64;
-  const int sub_begin = split * sub_per_split;
-  const int sub_end = min(nsub, sub_begin + sub_per_split);
-  const int nchunks = 2 * max(0, sub_end - sub_begin);
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  const int lrow = tid >> 2, lk = (tid & 3) * 8;
-  const bool xrow_ok = t0 + lrow < T, wrow_ok = e0 + lrow < E;
-  const __nv_bfloat16* xsrc = x + static_cast<size_t>(t0 + lrow) * D + lk;
-  const __nv_bfloat16* wsrc = wr + static_cast<size_t>(e0 + lrow) * D + lk;
-  uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
-  float xsq = 0.f, wsq = 0.f;
+struct RouterTcSmem {
+  uint8_t a[kRtStages][kRtE * 128];  // router rows, one k-block (128-B swizzle)
+  uint8_t b[kRtStages][kRtT * 128];  // token rows, one k-block
+  uint64_t full[kRtStages], empty[kRtStages];
+  uint64_t cfull[2], cempty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
 
-  auto gload = [&](int c) {
-    const int kbase = sub_begin * 64 + c * kRK;
-    if (xrow_ok) xv = __ldg(reinterpret_cast<const uint4*>(xsrc + kbase));
-    if (wrow_ok) wv = __ldg(reinterpret_cast<const uint4*>(wsrc + kbase));
-  };
-  auto sstore = [&](int buf) {
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float xl = __uint_as_float(xw[j] << 16), xh = __uint_as_float(xw[j] & 0xFFFF0000u);
-      const float wl = __uint_as_float(ww[j] << 16), wh = __uint_as_float(ww[j] & 0xFFFF0000u);
-      xs[buf][lk + 2 * j][lrow] = xl;
-      xs[buf][lk + 2 * j + 1][lrow] = xh;
-      ws[buf][lk + 2 * j][lrow] = wl;
-      ws[buf][lk + 2 * j + 1][lrow] = wh;
-      xsq = fmaf(xh, xh, fmaf(xl, xl, xsq));
-      wsq = fmaf(wh, wh, fmaf(wl, wl, wsq));
+__global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, int T,
+    int E, int nkb, int kbs, float* __restrict__ z_part, int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  RouterTcSmem& s =
+      *reinterpret_cast<RouterTcSmem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.x * kRtE, t0 = blockIdx.y * kRtT, sp = blockIdx.z;
+  const int kb_begin = sp * kbs;
+  const int nk = max(0, min(nkb, kb_begin + kbs) - kb_begin);
+  volatile int* abort_flag = &s.abort_flag;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRtStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.cfull[i], 1);
+      mbar_init(&s.cempty[i], 4);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_base;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    if (status) atomicCAS(status, 0, MOE_ERR_TIMEOUT);
   };
 
-  float acc[4][4], part[4][4];
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      uint32_t issued = 0, issued_ph = 0;
+      bool ok = true;
+      for (int c = 0; c < nk; ++c) {
+        const int st = c % kRtStages;
+        const uint32_t ph = (c / kRtStages) & 1u;
+        if (!mbar_wait(&s.empty[st], ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&s.full[st], (kRtE + kRtT) * 128);
+        issued |= 1u << st;
+        issued_ph = (issued_ph & ~(1u << st)) | (ph << st);
+        tma_load_2d(s.a[st], &tm_w, &s.full[st], (kb_begin + c) * 64, e0, pol);
+        tma_load_2d(s.b[st], &tm_x, &s.full[st], (kb_begin + c) * 64, t0, pol);
+      }
+      if (!ok) {
+        fail();
+        for (int i = 0; i < kRtStages; ++i)
+          if ((issued >> i) & 1u) mbar_wait_time_only_r(&s.full[i], (issued_ph >> i) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kRtE, kRtT);
+      bool ok = true;
+      for (int c = 0; c < nk; ++c) {
+        const int st = c % kRtStages, buf = c & 1;
+        if (!mbar_wait(&s.cempty[buf], ((c >> 1) & 1u) ^ 1u, abort_flag) ||
+            !mbar_wait(&s.full[st], (c / kRtStages) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = sdesc_sw128(smem_u32(s.a[st])), bd = sdesc_sw128(smem_u32(s.b[st]));
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tmem_base + static_cast<uint32_t>(buf * kRtT), ad + 2u * kk, bd + 2u * kk,
+                      idesc, kk != 0 ? 1u : 0u);
+        mma_commit(&s.empty[st]);
+        mma_commit(&s.cfull[buf]);
+      }
+      if (!ok) fail();
+      mma_commit(&s.drain);
+      mbar_wait_time_only_r(&s.drain, 0);
+    }
+  } else {
+    // epilogue: lane quarter warp % 4 holds experts e0 + 32 * (warp % 4) + lane
+    const int q = warp & 3;
+    const int e = e0 + 32 * q + lane;
+    float run[kRtT];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = part[i][j] = 0.f;
-
-  if (nchunks > 0) {
-    gload(0);
-    sstore(0);
+    for (int j = 0; j < kRtT; ++j) run[j] = 0.f;
+    bool ok = true;
+    for (int c = 0; c < nk; ++c) {
+      const int buf = c & 1;
+      if (!mbar_wait(&s.cfull[buf], (c >> 1) & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb =
+          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * kRtT);
+      uint32_t v[4][16];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tmem_ld_32x32b_x16(tb + 16u * g, v[g]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tmem_regs_ready(v[g]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.cempty[buf]);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) run[16 * g + j] += __uint_as_float(v[g][j]);
+    }
+    if (!ok) {
+      fail();
+    } else if (e < E) {
+      float* dst = z_part + static_cast<size_t>(sp) * T * E + e;
+#pragma unroll
+      for (int j = 0; j < kRtT; ++j)
+        if (t0 + j < T) dst[static_cast<size_t>(t0 + j) * E] = run[j];
+    }
   }
   __syncthreads();
-  for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    if (c + 1 < nchunks) gload(c + 1);
-#pragma unroll
-    for (int kk = 0; kk < kRK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
-    }
-    if (c & 1) {  // end of a 64-wide sub-chunk
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[i][j] += part[i][j];
-          part[i][j] = 0.f;
-        }
-    }
-    if (c + 1 < nchunks) sstore(buf ^ 1);
-    __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 128);
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-    float* dst = z_part + (static_cast<size_t>(split) * T + t) * E;
+}
+
+// Sums of squares of the token rows (xsq[t]) and router rows (wsq[e]), one warp
+// per row: each lane adds D/32 squares in order, then a five-step butterfly,
+// so every square passes through at most D/32 + 5 fp32 roundings.
+__global__ void __launch_bounds__(256) router_sumsq_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           const __nv_bfloat16* __restrict__ wr,
+                                                           int T, int E, int D,
+                                                           float* __restrict__ xsq,
+                                                           float* __restrict__ wsq) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= T + E) return;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      row < T ? x + static_cast<size_t>(row) * D : wr + static_cast<size_t>(row - T) * D);
+  float acc = 0.f;
+  for (int g = lane; g < D / 8; g += 32) {
+    const uint4 v = __ldg(src + g);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) dst[e] = acc[i][j];
+      const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      acc = fmaf(lo, lo, acc);
+      acc = fmaf(hi, hi, acc);
     }
   }
-  // four threads share each staged row: combine their squares
-  xsq += __shfl_xor_sync(0xffffffffu, xsq, 1);
-  xsq += __shfl_xor_sync(0xffffffffu, xsq, 2);
-  wsq += __shfl_xor_sync(0xffffffffu, wsq, 1);
-  wsq += __shfl_xor_sync(0xffffffffu, wsq, 2);
-  if ((tid & 3) == 0) {
-    if (blockIdx.x == 0 && xrow_ok) xsq_part[static_cast<size_t>(split) * T + t0 + lrow] = xsq;
-    if (blockIdx.y == 0 && wrow_ok) wsq_part[static_cast<size_t>(split) * E + e0 + lrow] = wsq;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    if (row < T)
+      xsq[row] = acc;
+    else
+      wsq[row - T] = acc;
   }
 }
 
@@ -273,35 +357,24 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   if (t >= T) return;
   const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
 
-  // ---- phase 1: split-K partials of the logits and of the squares, summed in
-  // split order; loads of four splits are issued before their additions.
+  // ---- phase 1: split-K partials of the logits, summed in split order (loads
+  // of four splits are issued before their additions); sums of squares.
   for (int e = tid; e < E; e += blockDim.x) {
-    float a = 0.f, b = 0.f;
+    float a = 0.f;
     int sp = 0;
     for (; sp + 4 <= S; sp += 4) {
-      float z4[4], w4[4];
+      float z4[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        z4[q] = __ldg(z_part + (static_cast<size_t>(sp + q) * T + t) * E + e);
-        w4[q] = __ldg(wsq_part + static_cast<size_t>(sp + q) * E + e);
-      }
+      for (int q = 0; q < 4; ++q) z4[q] = __ldg(z_part + (static_cast<size_t>(sp + q) * T + t) * E + e);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        a += z4[q];
-        b += w4[q];
-      }
+      for (int q = 0; q < 4; ++q) a += z4[q];
     }
-    for (; sp < S; ++sp) {
-      a += __ldg(z_part + (static_cast<size_t>(sp) * T + t) * E + e);
-      b += __ldg(wsq_part + static_cast<size_t>(sp) * E + e);
-    }
+    for (; sp < S; ++sp) a += __ldg(z_part + (static_cast<size_t>(sp) * T + t) * E + e);
     vs[e] = a;
-    wss[e] = b;
+    wss[e] = __ldg(wsq_part + e);
   }
   if (tid == 0) {
-    float xs = 0.f;
-    for (int sp = 0; sp < S; ++sp) xs += __ldg(xsq_part + static_cast<size_t>(sp) * T + t);
-    s_xsq = xs;
+    s_xsq = __ldg(xsq_part + t);
     s_ncand = 0;
   }
   __syncthreads();
@@ -567,36 +640,324 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   }
 }
 
+// Warp-per-token variant for large T (eight tokens per block): the same
+// decision as router_select_kernel, with the level-2 candidates of a token
+// recomputed one after another by its warp.
+template <int VPL>
+__global__ void __launch_bounds__(256) router_select_warp_kernel(
+    const float* __restrict__ z_part, int S, int T, int D, int E, int k,
+    const float* __restrict__ bias, const float* __restrict__ xsq_part,
+    const float* __restrict__ wsq_part, float gamma, const __nv_bfloat16* __restrict__ x,
+    const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
+    int* __restrict__ counters, float gamma2) {
+  extern __shared__ double zx_smem[];  // [8 warps][E] refined logits, then [8][64] uint4 staging
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + wib;
+  if (t >= T) return;
+  double* zx = zx_smem + static_cast<size_t>(wib) * E;
+  uint4* stage = reinterpret_cast<uint4*>(zx_smem + static_cast<size_t>(8) * E) + wib * 64;
+
+  float v[VPL], r[VPL], wn[VPL];
+  uint32_t sel = 0, cand = 0;
+  // Split-K partials of the logits summed in split order; the VPL loads of one
+  // split are independent and coalesced across the warp.
+  const float xsq = __ldg(xsq_part + t);
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = 0.f;
+    wn[i] = e < E ? __ldg(wsq_part + e) : 0.f;
+  }
+  for (int sp = 0; sp < S; ++sp) {
+    const float* zp = z_part + (static_cast<size_t>(sp) * T + t) * E;
+    float part[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      part[i] = e < E ? __ldg(zp + e) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] += part[i];
+  }
+  const float xn = norm_bound(xsq);
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    wn[i] = norm_bound(wn[i]);
+    if (e < E) {
+      if (bias) v[i] += __ldg(bias + e);
+      r[i] = gamma * xn * wn[i] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]);
+    } else {
+      v[i] = -INFINITY;
+      r[i] = 0.f;
+    }
+  }
+
+  // k rounds of warp arg-max under (value desc, index asc).
+  float min_lo = INFINITY;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((sel >> i) & 1u) && better(v[i], e, bv, be)) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) {
+      const int i = be >> 5;
+#pragma unroll
+      for (int q = 0; q < VPL; ++q)
+        if (q == i) {
+          sel |= 1u << q;
+          min_lo = fminf(min_lo, v[q] - r[q]);
+        }
+    }
+  }
+  float max_hi = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && !((sel >> i) & 1u)) max_hi = fmaxf(max_hi, v[i] + r[i]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    min_lo = fminf(min_lo, __shfl_xor_sync(0xffffffffu, min_lo, o));
+    max_hi = fmaxf(max_hi, __shfl_xor_sync(0xffffffffu, max_hi, o));
+  }
+
+  if (!(min_lo > max_hi)) {
+    // Not certified: experts whose interval reaches across the boundary.
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= E) continue;
+      const bool s_in = (sel >> i) & 1u;
+      if ((s_in && v[i] - r[i] <= max_hi) || (!s_in && v[i] + r[i] >= min_lo)) cand |= 1u << i;
+    }
+    int slots = __popc(sel & cand);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) slots += __shfl_xor_sync(0xffffffffu, slots, o);
+    if (lane == 0 && counters) atomicAdd(counters, 1);
+    const __nv_bfloat16* xr = x + static_cast<size_t>(t) * D;
+    // Level 2: compensated fp32 logits of every candidate, kept as the
+    // unevaluated pair (s, c) by the lane that owns the expert.
+    float zs[VPL], zc[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      zs[i] = zc[i] = 0.f;
+      uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
+      while (bal) {
+        const int src = __ffs(bal) - 1;
+        bal &= bal - 1;
+        const int e = src + 32 * i;
+        const float2 sc = warp_dot_comp(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane);
+        if (lane == src) {
+          zs[i] = sc.x;
+          zc[i] = sc.y;
+        }
+      }
+    }
+    // Values relative to a common reference (the largest candidate sum s):
+    // rel = (s - ref) + c, with |rel - (z - ref)| <= 2^-23 |rel| (s - ref is
+    // exact when s is within a factor of two of ref), all in fp32.
+    float ref = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if ((cand >> i) & 1u) ref = fmaxf(ref, zs[i]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ref = fmaxf(ref, __shfl_xor_sync(0xffffffffu, ref, o));
+    float rel[VPL], rad[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      rel[i] = -INFINITY;
+      rad[i] = 0.f;
+      if ((cand >> i) & 1u) {
+        rel[i] = (zs[i] - ref) + zc[i];
+        const float a = xn * wn[i] + (bias ? fabsf(bias[e]) : 0.f);
+        // gamma2 * sum|x w| (level-2 error, plus the fp64 definition's own
+        // distance from the exact sum) + rounding of rel and of rel -/+ rad
+        rad[i] = gamma2 * a * (1.0f + 0x1p-20f) + 0x1p-21f * fabsf(rel[i]);
+      }
+    }
+    uint32_t chosen = 0;
+    for (int j = 0; j < slots; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (((cand >> i) & 1u) && !((chosen >> i) & 1u) && better(rel[i], e, bv, be)) {
+          bv = rel[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (better(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+    }
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (!((cand >> i) & 1u)) continue;
+      if ((chosen >> i) & 1u)
+        lo = fminf(lo, rel[i] - rad[i]);
+      else
+        hi = fmaxf(hi, rel[i] + rad[i]);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    // Refined logits replace the fp32 ones for the weights.
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if ((cand >> i) & 1u) v[i] = zs[i] + zc[i];
+    if (!(lo > hi)) {
+      // Level 3: the defining index-order fp64 sum (exact ties end here).
+      if (lane == 0 && counters) atomicAdd(counters + 1, 1);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        uint32_t bal = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
+        while (bal) {
+          const int src = __ffs(bal) - 1;
+          bal &= bal - 1;
+          const int e = src + 32 * i;
+          const double z =
+              warp_exact_logit(xr, wr + static_cast<size_t>(e) * D, D, bias, e, lane, stage);
+          if (lane == src) zx[e] = z;
+        }
+      }
+      __syncwarp();
+      chosen = 0;
+      for (int j = 0; j < slots; ++j) {
+        double bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int e = lane + 32 * i;
+          if (((cand >> i) & 1u) && !((chosen >> i) & 1u) && better_d(zx[e], e, bv, be)) {
+            bv = zx[e];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (better_d(ov, oe, bv, be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+      }
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if ((cand >> i) & 1u) v[i] = static_cast<float>(zx[e]);
+      }
+    }
+    sel = (sel & ~cand) | chosen;
+  }
+
+  // Softmax over all E, renormalised over the selected k:
+  //   w_j = exp(v_j - m) / sum_selected exp(v_i - m)   (the full denominator cancels).
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float ex[VPL];
+  float den = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    ex[i] = ((sel >> i) & 1u) ? expf(v[i] - m) : 0.f;
+    den += ex[i];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+
+  // Ascending expert order: e = lane + 32 i, so scan i outer, lanes inner.
+  int32_t* out = blob + static_cast<size_t>(t) * 2 * k;
+  int base = 0;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const bool s_in = (sel >> i) & 1u;
+    const uint32_t bal = __ballot_sync(0xffffffffu, s_in);
+    if (s_in) {
+      const int pos = base + __popc(bal & lt_mask);
+      out[pos] = lane + 32 * i;
+      out[k + pos] = __float_as_int(ex[i] / den);
+    }
+    base += __popc(bal);
+  }
+}
+
+
 // ---------------------------------------------------------------- launchers
-void launch_router_logits(const void* x, const void* wr, int T, int D, int E, int S,
-                          int sub_per_split, float* z_part, float* xsq_part, float* wsq_part,
-                          cudaStream_t st) {
-  dim3 grid((E + kRE - 1) / kRE, (T + kRT - 1) / kRT, S);
-  router_logits_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                             static_cast<const __nv_bfloat16*>(wr), T, D, E,
-                                             sub_per_split, z_part, xsq_part, wsq_part);
+cudaError_t launch_router_logits_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                                    const void* x, const void* wr, int T, int D, int E, int S,
+                                    int kbs, float* z_part, float* xsq, float* wsq, int* status,
+                                    cudaStream_t st) {
+  router_sumsq_kernel<<<(T + E + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                                         static_cast<const __nv_bfloat16*>(wr),
+                                                         T, E, D, xsq, wsq);
+  const size_t smem = sizeof(RouterTcSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid((E + kRtE - 1) / kRtE, (T + kRtT - 1) / kRtT, S);
+  router_logits_tc_kernel<<<grid, 192, smem, st>>>(tm_w, tm_x, T, E, D / 64, kbs, z_part, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
                                  const float* bias, const float* xsq_part, const float* wsq_part,
                                  float gamma, float gamma2, const void* x, const void* wr,
                                  int32_t* blob, int* counters, cudaStream_t st) {
-  const int blocks = T;
-  const size_t smem = (static_cast<size_t>(E) * 28 + 15) / 16 * 16 + 64 * sizeof(uint4);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const auto* wb = static_cast<const __nv_bfloat16*>(wr);
-#define MOE_SELECT_CASE(V)                                                                   \
-  if (E <= 32 * (V)) {                                                                       \
-    if (smem > 48 * 1024) {                                                                  \
-      cudaError_t e_ = cudaFuncSetAttribute(router_select_kernel<V>,                         \
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,     \
-                                            static_cast<int>(smem));                         \
-      if (e_ != cudaSuccess) return e_;                                                      \
-    }                                                                                        \
-    router_select_kernel<V><<<blocks, 256, smem, st>>>(z_part, S, T, D, E, k, bias, xsq_part, \
-                                                       wsq_part, gamma, xb, wb, blob,        \
-                                                       counters, gamma2);                    \
-    return cudaGetLastError();                                                               \
+  // Up to ~2k tokens one block per token keeps every SM busy; above that a
+  // warp per token covers the batch in fewer waves.
+  const bool per_warp = T >= 2048;
+  const int blocks = per_warp ? (T + 7) / 8 : T;
+  const size_t smem =
+      per_warp ? static_cast<size_t>(8) * E * sizeof(double) + 8 * 64 * sizeof(uint4)
+               : (static_cast<size_t>(E) * 28 + 15) / 16 * 16 + 64 * sizeof(uint4);
+#define MOE_SELECT_CASE(V)                                                                    \
+  if (E <= 32 * (V)) {                                                                        \
+    auto kern = per_warp ? router_select_warp_kernel<V> : router_select_kernel<V>;            \
+    if (smem > 48 * 1024) {                                                                   \
+      cudaError_t e_ = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                            static_cast<int>(smem));                          \
+      if (e_ != cudaSuccess) return e_;                                                       \
+    }                                                                                         \
+    kern<<<blocks, 256, smem, st>>>(z_part, S, T, D, E, k, bias, xsq_part, wsq_part, gamma,   \
+                                    xb, wb, blob, counters, gamma2);                          \
+    return cudaGetLastError();                                                                \
   }
   MOE_SELECT_CASE(1)
   MOE_SELECT_CASE(4)

@@ -105,6 +105,44 @@ def test_route_near_ties_refined_exactly():
     assert refined > 0
 
 
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
+
+
+def test_router_logits_tensor_core_error_bound():
+    """The level-1 logits come from tensor-core MMAs whose fp32 accumulation is not
+    documented; routing certification assumes an error of at most 2^-15 sum|x w| per
+    64-wide K chunk.  Check the measured error against a bound twice as tight, on
+    plain inputs, on inputs whose magnitudes span 2^-12..2^12 within a row, and on
+    rows built to cancel (large equal-and-opposite products next to small ones)."""
+    T, D, E = 192, 1024, 256
+    cfg = MoEConfig("rl", T=T, D=D, E=E, I=64, Is=64, k=4)
+    rng = np.random.default_rng(7)
+    cases = []
+    x = rng.standard_normal((T, D)); w = rng.standard_normal((E, D)) * 0.02
+    cases.append((x, w))
+    xs = rng.standard_normal((T, D)) * 2.0 ** rng.integers(-12, 13, size=(T, D))
+    ws_ = rng.standard_normal((E, D)) * 2.0 ** rng.integers(-12, 13, size=(E, D))
+    cases.append((xs, ws_))
+    xc = np.repeat(rng.standard_normal((T, D // 2)) * 64.0, 2, axis=1)
+    wc = np.empty((E, D))
+    big = rng.standard_normal((E, D // 2)) * 64.0
+    wc[:, 0::2] = big
+    wc[:, 1::2] = -big + rng.standard_normal((E, D // 2)) * 2.0 ** -6
+    cases.append((xc, wc))
+    worst = 0.0
+    for xa, wa in cases:
+        xb, wb = _bf16(xa), _bf16(wa)
+        z = B.router_logits(cfg, xb.cuda(), wb.cuda()).cpu().double().numpy()
+        ref = oracle.router_logits(as_u16(xb), as_u16(wb))
+        a = np.abs(xb.double().numpy()) @ np.abs(wb.double().numpy()).T
+        bound = (2.0 ** -16 + (D / 64 + 2) * 2.0 ** -24) * a
+        err = np.abs(z - ref)
+        assert (err <= bound + 1e-30).all(), float((err / np.maximum(a, 1e-300)).max())
+        worst = max(worst, float((err / np.maximum(a, 1e-300)).max()))
+    print(f"worst |z - exact| / sum|x w| = {worst:.3e} (certification assumes 3.1e-05)")
+
+
 def test_route_with_bias():
     cfg = SMALL["hot"]
     host, dev = gpu_inputs(cfg)
