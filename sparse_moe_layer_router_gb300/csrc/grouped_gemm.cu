@@ -341,15 +341,26 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
   }
 }
 
-// Token tile of k-block kb with 32-row boxes (mb32) and, for a remainder of
-// 16 rows, one 16-row box (mb16): issuing a copy holds the issuing thread for
-// a few hundred cycles, so a tile takes as few copies as its rows allow.
-__device__ __forceinline__ void load_token_tile2(uint8_t* dst, const CUtensorMap* mb16,
-                                                 const CUtensorMap* mb32, uint64_t* bar,
-                                                 const TileInfo& t, int kb, uint64_t pol) {
+// Token tile of k-block kb from maps whose boxes are 16, 32, 64 and 128 rows
+// high (mb[0..3]): bn (a multiple of 16) is cut into its binary parts, largest
+// first, so a tile takes at most four copies (two for bn = 256).  Issuing a
+// copy holds the issuing thread for a few hundred cycles.
+__device__ __forceinline__ void load_token_tile_p2(uint8_t* dst, const CUtensorMap* const* mb,
+                                                   uint64_t* bar, const TileInfo& t, int kb,
+                                                   uint64_t pol) {
   int i = 0;
-  for (; i + 32 <= t.bn; i += 32) tma_load_2d(dst + i * 128, mb32, bar, kb * kBK, t.b_row + i, pol);
-  if (i < t.bn) tma_load_2d(dst + i * 128, mb16, bar, kb * kBK, t.b_row + i, pol);
+  while (i + 128 <= t.bn) {
+    tma_load_2d(dst + i * 128, mb[3], bar, kb * kBK, t.b_row + i, pol);
+    i += 128;
+  }
+#pragma unroll
+  for (int lg = 2; lg >= 0; --lg) {
+    const int rows = 16 << lg;
+    if (i + rows <= t.bn) {
+      tma_load_2d(dst + i * 128, mb[lg], bar, kb * kBK, t.b_row + i, pol);
+      i += rows;
+    }
+  }
 }
 
 // Token tile of k-block kb: bn rows of 64 K in 16-row boxes (128-B swizzle).
@@ -369,7 +380,11 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
                         const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_b_s,
                         const __grid_constant__ CUtensorMap tm_b2,
-                        const __grid_constant__ CUtensorMap tm_b2_s, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tm_b2_s,
+                        const __grid_constant__ CUtensorMap tm_b4,
+                        const __grid_constant__ CUtensorMap tm_b4_s,
+                        const __grid_constant__ CUtensorMap tm_b8,
+                        const __grid_constant__ CUtensorMap tm_b8_s, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = Bf16Smem<BN_MAX, STAGES>;
   const uint32_t raw = smem_u32(smem_raw);
@@ -392,10 +407,14 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
     prefetch_tmap(&tm_b2);
+    prefetch_tmap(&tm_b4);
+    prefetch_tmap(&tm_b8);
     if (p.has_shared) {
       prefetch_tmap(&tm_a_s);
       prefetch_tmap(&tm_b_s);
       prefetch_tmap(&tm_b2_s);
+      prefetch_tmap(&tm_b4_s);
+      prefetch_tmap(&tm_b8_s);
     }
   }
   const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kBaseThreads);
@@ -422,8 +441,9 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
         const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
         const CUtensorMap* ma = t.shared ? &tm_a_s : &tm_a;
-        const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
-        const CUtensorMap* mb2 = t.shared ? &tm_b2_s : &tm_b2;
+        const CUtensorMap* const mb[4] = {t.shared ? &tm_b_s : &tm_b, t.shared ? &tm_b2_s : &tm_b2,
+                                          t.shared ? &tm_b4_s : &tm_b4,
+                                          t.shared ? &tm_b8_s : &tm_b8};
         const uint32_t bytes = kAStage + static_cast<uint32_t>(t.bn) * 128u;
         const int row = tile_a_row(p, t);
         for (int kb = 0; kb < t.k_blocks; ++kb) {
@@ -438,7 +458,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
             tma_load_4d(s.a[stage], ma, &s.full[stage], kb * kBK, 0, 0, row / 16, pol_w);
           else
             tma_load_2d(s.a[stage], ma, &s.full[stage], kb * kBK, row, pol_w);
-          load_token_tile2(s.b[stage], mb, mb2, &s.full[stage], t, kb, pol_x);
+          load_token_tile_p2(s.b[stage], mb, &s.full[stage], t, kb, pol_x);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -1216,7 +1236,8 @@ static cudaError_t launch_bf16(const GemmParams& p, const GemmMaps& m, int num_s
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kBaseThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.b2, m.b2_s, p);
+  kern<<<num_sms, kBaseThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.b2, m.b2_s, m.b4, m.b4_s,
+                                             m.b8, m.b8_s, p);
   return cudaGetLastError();
 }
 

@@ -389,12 +389,20 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     ok &= w4 ? map_gate_up_i4(&maps.a, a->w, c->E, c->I, c->D)
              : map_gate_up_bf16_4d(&maps.a, a->w, c->E, c->I, c->D);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, tok_rows);
-    if (!w4) ok &= map_2d_bf16(&maps.b2, b_routed, P, c->D, 32);
+    if (!w4) {
+      ok &= map_2d_bf16(&maps.b2, b_routed, P, c->D, 32);
+      ok &= map_2d_bf16(&maps.b4, b_routed, P, c->D, 64);
+      ok &= map_2d_bf16(&maps.b8, b_routed, P, c->D, 128);
+    }
     if (has_shared) {
       ok &= w4 ? map_gate_up_i4(&maps.a_s, a->w_shared, 1, c->I_shared, c->D)
                : map_gate_up_bf16_4d(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->D, tok_rows);
-      if (!w4) ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->D, 32);
+      if (!w4) {
+        ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->D, 32);
+        ok &= map_2d_bf16(&maps.b4_s, a->a_shared, c->T, c->D, 64);
+        ok &= map_2d_bf16(&maps.b8_s, a->a_shared, c->T, c->D, 128);
+      }
     }
   } else {
     p.m_tiles = c->D / 128;
@@ -407,12 +415,20 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     ok &= w4 ? map_2d_i4(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128)
              : map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, tok_rows);
-    if (!w4) ok &= map_2d_bf16(&maps.b2, b_routed, P, c->I, 32);
+    if (!w4) {
+      ok &= map_2d_bf16(&maps.b2, b_routed, P, c->I, 32);
+      ok &= map_2d_bf16(&maps.b4, b_routed, P, c->I, 64);
+      ok &= map_2d_bf16(&maps.b8, b_routed, P, c->I, 128);
+    }
     if (has_shared) {
       ok &= w4 ? map_2d_i4(&maps.a_s, a->w_shared, c->D, c->I_shared, 128)
                : map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, tok_rows);
-      if (!w4) ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->I_shared, 32);
+      if (!w4) {
+        ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->I_shared, 32);
+        ok &= map_2d_bf16(&maps.b4_s, a->a_shared, c->T, c->I_shared, 64);
+        ok &= map_2d_bf16(&maps.b8_s, a->a_shared, c->T, c->I_shared, 128);
+      }
     }
   }
   // W4A16 scale tables by TMA when every K of the launch is a multiple of 1024
@@ -429,12 +445,12 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     }
   }
   if (!ok) return MOE_ERR_CUDA;
-  if (w4) maps.b2 = maps.b;
+  if (w4) maps.b2 = maps.b4 = maps.b8 = maps.b;
   if (!has_shared) {
     maps.a_s = maps.a;
     maps.b_s = maps.b;
   }
-  if (w4 || !has_shared) maps.b2_s = maps.b_s;
+  if (w4 || !has_shared) maps.b2_s = maps.b4_s = maps.b8_s = maps.b_s;
   if (!p.scale_table || !has_shared) maps.sc_s = maps.a_s;
   if (!p.scale_table) maps.sc = maps.a;
   return cuda_rc(launch_grouped_gemm(p, maps, bn_max, c->quant, dev.sms, st));

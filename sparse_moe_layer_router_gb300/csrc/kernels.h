@@ -73,6 +73,8 @@ struct GemmMaps {
   CUtensorMap a, a_s, b, b_s;  // weights (routed, shared), activations (routed, shared)
   CUtensorMap sc, sc_s;        // W4A16 group scales (routed, shared)
   CUtensorMap b2, b2_s;        // bf16 kernels: activations in 32-row boxes (b, b_s: 16 rows)
+  CUtensorMap b4, b4_s;        //               64-row boxes
+  CUtensorMap b8, b8_s;        //               128-row boxes
 };
 
 // Kernel variants: BN_MAX token rows per tile (64 or 256); quant 0 = bf16, 1 = W4A16.
