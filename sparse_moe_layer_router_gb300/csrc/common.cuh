@@ -44,30 +44,52 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// With a suspend-time hint a waiting thread may sleep (up to 1 ms) instead of
+// spinning, so waiting warps leave the issue slots to the working ones; it
+// resumes when the phase completes.  Without the hint the wait returns after
+// the hardware's default time, which wakes a little sooner after completion.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if (kSleep) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 // Waits for the phase with `parity` to complete.  Returns false (without
 // completing) if *abort becomes non-zero or `limit_ns` of global time passes.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kSleep>(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kSleep>(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (*abort) return false;
       if (globaltimer() - t0 > limit_ns) return false;
     }
   }
+}
+// Long waits off the critical path (an epilogue waiting for a whole tile):
+// sleep so the spinning warp does not take issue slots from the producers.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort) {
+  return mbar_wait<true>(bar, parity, abort);
 }
 
 // Waits with only the time bound (used while unwinding after an abort).

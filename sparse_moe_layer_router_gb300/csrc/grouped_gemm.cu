@@ -251,7 +251,7 @@ __device__ __forceinline__ void init_common_barriers(GemmCommon<BN_MAX>& c) {
 // Epilogue role (warps 2-5): TMEM accumulators -> h (SwiGLU, bf16) or o
 // (routing-weighted, fp32).  With NP = 2 the accumulator is the sum of two
 // partial accumulators 2 * BN_MAX columns apart (two MMA issuers).
-template <int BN_MAX, int NP = 1>
+template <int BN_MAX, int NP = 1, bool kSleep = false>
 __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G, int ntiles,
                               uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
   const int sp = warp & 3;  // TMEM lanes 32*sp .. 32*sp+31
@@ -277,7 +277,7 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
       }
       __syncwarp();
     }
-    if (!mbar_wait(&s.tfull[acc], acc_phase, abort_flag)) {
+    if (!mbar_wait<kSleep>(&s.tfull[acc], acc_phase, abort_flag)) {
       record_error(p, abort_flag, MOE_ERR_TIMEOUT);
       break;
     }
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
         const uint32_t bytes = kAStage + static_cast<uint32_t>(t.bn) * 128u;
         const int row = tile_a_row(p, t);
         for (int kb = 0; kb < t.k_blocks; ++kb) {
-          if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
+          if (!mbar_wait<true>(&s.empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
         const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
-        if (!mbar_wait(&cm.tempty[acc], acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait<true>(&cm.tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN_MAX);
         const uint32_t idesc = idesc_bf16_f32(kBM, t.bn);
         for (int kb = 0; kb < t.k_blocks; ++kb) {
-          if (!mbar_wait(&s.full[stage], phase, abort_flag)) {
+          if (!mbar_wait<true>(&s.full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
       mbar_wait_time_only(&cm.drain, 0);
     }
   } else {
-    epilogue_role<BN_MAX>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
+    epilogue_role<BN_MAX, 1, true>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
   }
 
   __syncthreads();
