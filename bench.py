@@ -348,7 +348,9 @@ def main():
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
     value = world * cfg.T * args.steps / (ms_total / 1e3)
-    launches_per_step = 10  # sums of squares, logits, select, count, scan, scatter, gather, 2 GEMMs, combine
+    # sums of squares, logits, select, dispatch (one block up to 4096 pairs, else
+    # count + scan + scatter), gather, 2 GEMMs, combine
+    launches_per_step = 8 if cfg.T * cfg.k <= 4096 else 10
 
     # ---------------- the path split into its ABI calls, events around each call
     blob = torch.empty((cfg.T, 2, cfg.k), dtype=torch.int32, device=dev)

@@ -145,10 +145,99 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = __ldg(s + i);
 }
 
+// Small problems in one block of 1024 threads (one launch instead of three):
+// warp w owns pairs [w*seg, (w+1)*seg); per-warp expert counts in shared
+// memory, one block-wide scan over experts, then each warp places its pairs
+// in order exactly as permute_scatter_kernel does.  Same results.
+constexpr int kPermuteOneBlockMaxPairs = 4096;
+__global__ void __launch_bounds__(1024) permute_one_block_kernel(
+    const int32_t* __restrict__ blob, int P, int k, int E, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ perm_pair, int32_t* __restrict__ inv_row) {
+  extern __shared__ int wc[];  // [32][E], then [32] warp sums
+  int* warp_sums = wc + 32 * E;
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wc[i] = 0;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int seg = (P + 31) / 32;
+  const int p0 = wid * seg, p1 = min(P, p0 + seg);
+  for (int p = p0 + lane; p < p1; p += 32) atomicAdd(&wc[wid * E + pair_expert(blob, k, p)], 1);
+  __syncthreads();
+  for (int e0 = 0; e0 < E; e0 += 1024) {
+    const int e = e0 + threadIdx.x;
+    int total = 0;
+    if (e < E)
+      for (int w = 0; w < 32; ++w) total += wc[w * E + e];
+    int incl = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int v = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      warp_sums[lane] = v;
+    }
+    __syncthreads();
+    const int excl = carry + (wid ? warp_sums[wid - 1] : 0) + incl - total;
+    if (e < E) {
+      counts[e] = total;
+      offsets[e] = excl;
+      int run = excl;
+      for (int w = 0; w < 32; ++w) {
+        const int c = wc[w * E + e];
+        wc[w * E + e] = run;
+        run += c;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry += warp_sums[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) offsets[E] = carry;
+  int* my = wc + wid * E;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const bool valid = p < p1;
+    const int e = valid ? pair_expert(blob, k, p) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int pos = 0;
+    if (valid) pos = my[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0) my[e] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      perm_pair[pos] = p;
+      inv_row[p] = pos;
+    }
+  }
+}
+
 cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,
                            int32_t* counts, int32_t* offsets, int32_t* perm_pair,
                            int32_t* inv_row, cudaStream_t st) {
   const int P = T * k;
+  const size_t smem_one = (static_cast<size_t>(32) * E + 32) * sizeof(int);
+  if (P <= kPermuteOneBlockMaxPairs && smem_one <= 200 * 1024) {
+    if (smem_one > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(permute_one_block_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem_one));
+      if (e != cudaSuccess) return e;
+    }
+    permute_one_block_kernel<<<1, 1024, smem_one, st>>>(blob, P, k, E, counts, offsets, perm_pair,
+                                                        inv_row);
+    return cudaGetLastError();
+  }
   const int B = (P + kPermuteChunk - 1) / kPermuteChunk;
   const size_t smem_count = static_cast<size_t>(E) * sizeof(int);
   const size_t smem_scatter = static_cast<size_t>(8) * E * sizeof(int);
