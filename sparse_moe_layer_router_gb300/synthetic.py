@@ -68,6 +68,10 @@ CONFIGS = {
     # W4A16 with ~20 token rows per expert (as in the T=1024 prefill) on 64 experts
     # (0.42 GB of packed weights): the W4A16 hardware-counter capture case.
     "w4a16_e64": MoEConfig("w4a16_e64", T=128, D=4096, E=64, I=1024, Is=1024, k=10, quant=1),
+    # Zipf-biased routing at T=2048 (256-row token tiles) on 64 experts (1.6 GB of
+    # weights): the hardware-counter capture case of the skewed kernel shape.
+    "skewed_e64": MoEConfig("skewed_e64", T=2048, D=4096, E=64, I=1024, Is=1024, k=10,
+                            zipf_s=1.2, zipf_alpha=0.9492),
 }
 
 _TAG_X, _TAG_WR, _TAG_RANK = 1, 2, 3
