@@ -359,19 +359,29 @@ __global__ void __launch_bounds__(256) router_select_kernel(
 
   // ---- phase 1: split-K partials of the logits, summed in split order (loads
   // of four splits are issued before their additions); sums of squares.
-  for (int e = tid; e < E; e += blockDim.x) {
-    float a = 0.f;
-    int sp = 0;
-    for (; sp + 4 <= S; sp += 4) {
-      float z4[4];
+  // Up to 16 splits (the host plan's cap) x 2 experts per thread: every load
+  // is issued before the first addition, so one memory latency covers them.
+  for (int e0 = 0; e0 < E; e0 += 2 * 256) {
+    float z[2][16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) z4[q] = __ldg(z_part + (static_cast<size_t>(sp + q) * T + t) * E + e);
+    for (int j = 0; j < 2; ++j) {
+      const int e = e0 + tid + 256 * j;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) a += z4[q];
+      for (int sp = 0; sp < 16; ++sp)
+        z[j][sp] = (e < E && sp < S) ? __ldg(z_part + (static_cast<size_t>(sp) * T + t) * E + e)
+                                     : 0.f;
     }
-    for (; sp < S; ++sp) a += __ldg(z_part + (static_cast<size_t>(sp) * T + t) * E + e);
-    vs[e] = a;
-    wss[e] = __ldg(wsq_part + e);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int e = e0 + tid + 256 * j;
+      if (e >= E) continue;
+      float a = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < 16; ++sp)
+        if (sp < S) a += z[j][sp];
+      vs[e] = a;
+      wss[e] = __ldg(wsq_part + e);
+    }
   }
   if (tid == 0) {
     s_xsq = __ldg(xsq_part + t);
