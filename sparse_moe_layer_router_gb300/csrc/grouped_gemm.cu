@@ -15,16 +15,20 @@
 //     with few tokens still streams full-width weight tiles.
 //   * warp 0: TMA producer (one thread); warp 1: TMEM allocation and
 //     tcgen05.mma issue (one thread), fp32 accumulators in TMEM, double
-//     buffered; warps 2-5: epilogue (tcgen05.ld); W4A16 adds warps 6-13, which
-//     restore packed int4 tiles to the bf16 operand in shared memory.
+//     buffered; warps 2-5: epilogue (tcgen05.ld).  The W4A16 kernels add
+//     dequant warps that restore the packed int4 tiles (into the shared-memory
+//     operand for 256-row token tiles, into tensor memory for tiles of up to 64
+//     rows) and a token-row producer warp; the TMEM variant has a second MMA
+//     warp.
 //   * Tiles: every CTA walks tile indices blockIdx.x, +gridDim.x, ... over the
 //     concatenation of groups [shared, expert 0, ..., expert E-1]; a group with
 //     R rows has ceil(R / BN_MAX) * m_tiles tiles, token tiles of one weight
 //     tile adjacent so repeated weight tiles come from L2.
 //   * Gate/up: a tile covers 64 output features; its A rows are four blocks of
-//     (16 gate rows, 16 up rows) loaded by a 3-D TMA box, so each epilogue warp
-//     holds gate and up of the same 16 features in its TMEM lanes and forms
-//     h = silu(g) * u with one lane exchange (no shared memory, no barrier).
+//     (16 gate rows, 16 up rows) (one 4-D TMA box for bf16, four 3-D boxes for
+//     int4), so each epilogue warp holds gate and up of the same 16 features in
+//     its TMEM lanes and forms h = silu(g) * u with one lane exchange (no
+//     shared memory, no barrier).
 //   * Down: a tile covers 128 output features; the epilogue multiplies by the
 //     routing weight of the row's (token, slot) pair and stores fp32.
 //   * Every wait is bounded (2 s); on expiry the CTA records MOE_ERR_TIMEOUT,
@@ -41,9 +45,10 @@ constexpr int kMaxGroups = 1025;
 constexpr int kBaseThreads = 192;       // producer, MMA, 4 epilogue warps
 
 // W4A16: packed stages of 128 rows x 128 B (256 int4 values = 4 k-blocks).
-// Two dequant groups of four warps (one tile row per thread); group g restores
-// k-blocks 4q + g and 4q + 2 + g of packed stage q into its two operand
-// buffers 2g and 2g + 1, so it restores one while the MMA reads the other.
+// Shared-memory variant: two dequant groups of four warps (one tile row per
+// thread); group g restores k-blocks 4q + g and 4q + 2 + g of packed stage q
+// into its two operand buffers 2g and 2g + 1, so it restores one while the MMA
+// reads the other.
 constexpr int kPackedK = 256;
 constexpr int kPackedStage = kBM * kPackedK / 2;  // 16 KB
 constexpr int kKPerPacked = kPackedK / kBK;       // 4 k-blocks per packed stage

@@ -220,9 +220,9 @@ __global__ void __launch_bounds__(256) router_sumsq_kernel(const __nv_bfloat16* 
 }
 
 // ---------------------------------------------------------------- select
-// Upper bound of a Euclidean norm from split partial sums of squares: the fp32
-// sums pass each square through at most D/4 + S + 2 roundings (relative error
-// below 2^-9 for D <= 65536); sqrt and the products add 2^-20 of slack.
+// Upper bound of a Euclidean norm from an fp32 sum of squares: each square
+// passes through at most D/32 + 5 roundings (router_sumsq_kernel), relative
+// error below 2^-9 for D <= 65536; sqrt and the products add 2^-20 of slack.
 __device__ __forceinline__ float norm_bound(float sumsq) {
   return sqrtf(sumsq * (1.0f + 0x1p-9f)) * (1.0f + 0x1p-20f);
 }
