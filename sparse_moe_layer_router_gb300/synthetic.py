@@ -68,6 +68,12 @@ CONFIGS = {
     # W4A16 with ~20 token rows per expert (as in the T=1024 prefill) on 64 experts
     # (0.42 GB of packed weights): the W4A16 hardware-counter capture case.
     "w4a16_e64": MoEConfig("w4a16_e64", T=128, D=4096, E=64, I=1024, Is=1024, k=10, quant=1),
+    # W4A16 at the decode batch (T=64): ~370 touched experts, 1-6 rows each.
+    "w4a16_decode": MoEConfig("w4a16_decode", T=64, D=4096, E=512, I=1024, Is=1024, k=10,
+                              quant=1, group=128),
+    # Compute-bound grouped GEMM: T=8192 on 64 experts, ~1280 rows per expert
+    # (256-row token tiles), where the tensor pipe rather than HBM bounds the GEMMs.
+    "dense_e64": MoEConfig("dense_e64", T=8192, D=4096, E=64, I=1024, Is=1024, k=10),
     # Zipf-biased routing at T=2048 (256-row token tiles) on 64 experts (1.6 GB of
     # weights): the hardware-counter capture case of the skewed kernel shape.
     "skewed_e64": MoEConfig("skewed_e64", T=2048, D=4096, E=64, I=1024, Is=1024, k=10,
