@@ -60,7 +60,7 @@ def parse():
 
 def workload_desc(cfg):
     d = (f"{cfg.name}: T={cfg.T}, D={cfg.D}, E={cfg.E}, I={cfg.I}, Is={cfg.Is}, top-{cfg.k}, "
-         f"{'W4A16 int4 g128' if cfg.quant else 'bf16'} weights")
+         f"{('W4A16 int4 ' + ('channel-wise' if cfg.group == 0 else f'g{cfg.group}')) if cfg.quant else 'bf16'} weights")
     if cfg.zipf_s:
         d += f", log-Zipf(s={cfg.zipf_s}) router bias x{cfg.zipf_alpha}"
     return d
@@ -122,6 +122,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
+def scales_per_row(cfg, K):
+    """bf16 scales per weight row of length K: K / group, or 1 (channel-wise, group 0)."""
+    return 1 if cfg.group == 0 else K // cfg.group
+
+
 def touched_gate_up_bytes(cfg, counts):
     """Algorithmic HBM bytes of one grouped gate/up launch (see DESIGN)."""
     import torch
@@ -131,8 +136,8 @@ def touched_gate_up_bytes(cfg, counts):
         w_exp = 2 * cfg.I * cfg.D * 2
         w_sh = 2 * cfg.Is * cfg.D * 2
     else:
-        w_exp = 2 * cfg.I * cfg.D // 2 + 2 * cfg.I * (cfg.D // cfg.group) * 2
-        w_sh = 2 * cfg.Is * cfg.D // 2 + 2 * cfg.Is * (cfg.D // cfg.group) * 2
+        w_exp = 2 * cfg.I * cfg.D // 2 + 2 * cfg.I * scales_per_row(cfg, cfg.D) * 2
+        w_sh = 2 * cfg.Is * cfg.D // 2 + 2 * cfg.Is * scales_per_row(cfg, cfg.D) * 2
     act = P * cfg.D * 2 + cfg.T * cfg.D * 2 + P * cfg.I * 2 + cfg.T * cfg.Is * 2
     del torch
     return touched * w_exp + w_sh + act, touched
@@ -144,8 +149,11 @@ def layer_bytes_flops(cfg, touched):
         per_exp = 3 * cfg.I * cfg.D * 2
         sh = 3 * cfg.Is * cfg.D * 2
     else:
-        per_exp = 3 * cfg.I * cfg.D // 2 + 3 * cfg.I * (cfg.D // cfg.group) * 2
-        sh = 3 * cfg.Is * cfg.D // 2 + 3 * cfg.Is * (cfg.D // cfg.group) * 2
+        # gate/up rows of length D and down rows of length I (or Is)
+        per_exp = (3 * cfg.I * cfg.D // 2 + 2 * cfg.I * scales_per_row(cfg, cfg.D) * 2
+                   + cfg.D * scales_per_row(cfg, cfg.I) * 2)
+        sh = (3 * cfg.Is * cfg.D // 2 + 2 * cfg.Is * scales_per_row(cfg, cfg.D) * 2
+              + cfg.D * scales_per_row(cfg, cfg.Is) * 2)
     byts = touched * per_exp + sh + cfg.E * cfg.D * 2 + 2 * cfg.T * cfg.D * 2
     flops = (2 * cfg.T * cfg.D * cfg.E + 6 * cfg.T * cfg.k * cfg.D * cfg.I
              + 6 * cfg.T * cfg.D * cfg.Is)

@@ -66,7 +66,9 @@ extern "C" {
 #define MOE_QUANT_BF16 0    /* bf16 expert weights                                   */
 #define MOE_QUANT_W4A16 1   /* symmetric int4, 8 per int32 in pair order (value 2i
                                in bits 4i..4i+3, value 2i+1 in bits 16+4i..19+4i,
-                               two's complement), bf16 scale per `group` K values [R1] */
+                               two's complement); bf16 scales, one per `group` = 128
+                               K values ([rows][K/128]) or, with group = 0, one per
+                               output row ([rows], channel-wise) [R1] */
 
 /* ---- grouped GEMM operations ---- */
 #define MOE_OP_GATE_UP_SWIGLU 0  /* h = silu(a.Wg^T) * (a.Wu^T) -> bf16               */
@@ -84,8 +86,9 @@ extern "C" {
  *   T        tokens (1 .. 2^20), D hidden size (multiple of 128),
  *   E        routed experts (1 .. 1024), I / I_shared expert intermediate sizes
  *            (multiples of 64), k experts per token (1 .. min(E, 32)),
- *   quant    MOE_QUANT_*; for W4A16, group = 128 and D, I, I_shared are
- *            multiples of 256 (packed K tiles of 256 values).
+ *   quant    MOE_QUANT_*; for W4A16, group = 128 (group scales) or 0
+ *            (channel-wise scales), and D, I, I_shared are multiples of 256
+ *            (packed K tiles of 256 values).
  */
 typedef struct moe_config {
   int T, D, E, I, I_shared, k;
@@ -100,7 +103,8 @@ typedef struct moe_config {
  *   quant == BF16 : w_gate_up bf16 [E][2I][D], w_down bf16 [E][D][I];
  *                   scale pointers must be NULL.
  *   quant == W4A16: w_gate_up int32 [E][2I][D/8] + s_gate_up bf16 [E][2I][D/group],
- *                   w_down int32 [E][D][I/8] + s_down bf16 [E][D][I/group].
+ *                   w_down int32 [E][D][I/8] + s_down bf16 [E][D][I/group];
+ *                   with group = 0: s_gate_up bf16 [E][2I], s_down bf16 [E][D].
  *   The shared expert (ws_*, ss_*) has the same format with I_shared and no
  *   leading E.  w_router is bf16 [E][D] in both cases; router_bias is fp32 [E]
  *   or NULL.

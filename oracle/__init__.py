@@ -157,7 +157,8 @@ def permute(ids, E):
 
 
 def dequant_w4(q, s, group):
-    """Exact fp64 value of a packed int4 matrix: q [R, C/8] int32, s [R, C/group] bf16."""
+    """Exact fp64 value of a packed int4 matrix: q [R, C/8] int32, s [R, C/group] bf16
+    (group 0: channel-wise, s [R] or [R, 1])."""
     q = _c(q, np.int32)
     s = _c(s, np.uint16)
     R = q.shape[0]

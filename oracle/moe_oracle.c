@@ -49,7 +49,9 @@
  *  R7  int4 packing: 8 values per int32 along K, in pair order: value 2i of
  *      the 8 in bits [4i, 4i+4) and value 2i+1 in bits [16+4i, 20+4i)
  *      (i = 0..3), two's complement.  Scale: one bf16 per (row, group of
- *      `group` consecutive K).  Dequantised weight = q * s, exact in fp64.
+ *      `group` consecutive K); group 0 means channel-wise, one scale per row
+ *      (the release note's other supported scale strategy).  Dequantised
+ *      weight = q * s, exact in fp64.
  *  R8  Everything after routing is computed in fp64 with no intermediate
  *      rounding.
  *
@@ -89,8 +91,11 @@ typedef struct {
   int rows, cols, quant, group;
   const uint16_t *bf16;  /* quant == 0: [rows][cols]             */
   const int32_t *q;      /* quant == 1: [rows][cols/8]           */
-  const uint16_t *s;     /* quant == 1: [rows][cols/group] bf16  */
+  const uint16_t *s;     /* quant == 1: [rows][cols/group] bf16 (group 0: [rows]) */
 } wview;
+
+/* Scales per row: cols/group, or 1 for channel-wise scales (group 0). */
+static int group_len(const wview *w) { return w->group > 0 ? w->group : w->cols; }
 
 /* Row `r` of W as fp64 values (dequantised exactly when quant == 1). */
 static void load_row(const wview *w, int r, double *out) {
@@ -98,10 +103,11 @@ static void load_row(const wview *w, int r, double *out) {
     const uint16_t *p = w->bf16 + (size_t)r * w->cols;
     for (int c = 0; c < w->cols; ++c) out[c] = bf16_to_f64(p[c]);
   } else {
+    const int g = group_len(w);
     const int32_t *q = w->q + (size_t)r * (w->cols / 8);
-    const uint16_t *s = w->s + (size_t)r * (w->cols / w->group);
+    const uint16_t *s = w->s + (size_t)r * (w->cols / g);
     for (int c = 0; c < w->cols; ++c)
-      out[c] = (double)nibble_s4(q[c / 8], c % 8) * bf16_to_f64(s[c / w->group]);
+      out[c] = (double)nibble_s4(q[c / 8], c % 8) * bf16_to_f64(s[c / g]);
   }
 }
 
@@ -272,7 +278,8 @@ int oracle_permute(int T, int E, int k, const int32_t *ids, int32_t *counts,
 /* ------------------------------------------------------------------ */
 int oracle_dequant_w4(int rows, int cols, int group, const int32_t *q,
                       const uint16_t *s, double *out) {
-  if (rows < 0 || cols < 8 || cols % 8 || group < 1 || cols % group || !q || !s || !out)
+  if (rows < 0 || cols < 8 || cols % 8 || group < 0 || (group > 0 && cols % group) || !q ||
+      !s || !out)
     return ORACLE_EINVAL;
   wview v = {rows, cols, 1, group, NULL, q, s};
   for (int r = 0; r < rows; ++r) load_row(&v, r, out + (size_t)r * cols);
@@ -309,6 +316,7 @@ static void expert_ffn(const wview *gu, const wview *dn, int D, int Ie,
  *   quant == 0: w_gu[e] -> bf16 [2Ie][D], w_dn[e] -> bf16 [D][Ie]
  *   quant == 1: w_gu[e] -> int32 [2Ie][D/8], s_gu[e] -> bf16 [2Ie][D/group],
  *               w_dn[e] -> int32 [D][Ie/8], s_dn[e] -> bf16 [D][Ie/group]
+ *               (group 0: s_gu[e] -> bf16 [2Ie], s_dn[e] -> bf16 [D])
  * with Ie = I for routed experts and Is for the shared one.
  */
 int oracle_forward(int nt, int D, int E, int I, int Is, int k, int quant,
@@ -318,8 +326,9 @@ int oracle_forward(int nt, int D, int E, int I, int Is, int k, int quant,
   if (nt < 0 || D < 1 || E < 1 || I < 1 || Is < 1 || k < 1 || k > E || !x ||
       !ids || !w || !w_gu || !w_dn || !y)
     return ORACLE_EINVAL;
-  if (quant == 1 && (!s_gu || !s_dn || group < 1 || D % group || I % group ||
-                     Is % group || D % 8 || I % 8 || Is % 8))
+  if (quant == 1 && (!s_gu || !s_dn || group < 0 ||
+                     (group > 0 && (D % group || I % group || Is % group)) || D % 8 ||
+                     I % 8 || Is % 8))
     return ORACLE_EINVAL;
   for (int t = 0; t < nt; ++t)
     for (int j = 0; j < k; ++j) {
@@ -387,7 +396,8 @@ int oracle_expert_hidden(int n, int D, int Ie, int quant, int group,
                          const uint16_t *x, const void *w_gu, const uint16_t *s_gu,
                          double *h) {
   if (n < 0 || D < 1 || Ie < 1 || !x || !w_gu || !h) return ORACLE_EINVAL;
-  if (quant == 1 && (!s_gu || group < 1 || D % group || D % 8)) return ORACLE_EINVAL;
+  if (quant == 1 && (!s_gu || group < 0 || (group > 0 && D % group) || D % 8))
+    return ORACLE_EINVAL;
   wview gu = {2 * Ie, D, quant, group, NULL, NULL, NULL};
   if (quant == 0) gu.bf16 = (const uint16_t *)w_gu;
   else { gu.q = (const int32_t *)w_gu; gu.s = s_gu; }
@@ -421,7 +431,8 @@ int oracle_expert_hidden(int n, int D, int Ie, int quant, int group,
 int oracle_expert_down(int n, int D, int Ie, int quant, int group, const double *h,
                        const void *w_dn, const uint16_t *s_dn, double *o) {
   if (n < 0 || D < 1 || Ie < 1 || !h || !w_dn || !o) return ORACLE_EINVAL;
-  if (quant == 1 && (!s_dn || group < 1 || Ie % group || Ie % 8)) return ORACLE_EINVAL;
+  if (quant == 1 && (!s_dn || group < 0 || (group > 0 && Ie % group) || Ie % 8))
+    return ORACLE_EINVAL;
   wview dn = {D, Ie, quant, group, NULL, NULL, NULL};
   if (quant == 0) dn.bf16 = (const uint16_t *)w_dn;
   else { dn.q = (const int32_t *)w_dn; dn.s = s_dn; }

@@ -194,6 +194,8 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 // the low bits of the two halves; XOR with 8 makes them offset binary (q + 8)
 // and 0x4300 | u is the bf16 of 128 + u (exact); subtracting 136 (exact) and
 // multiplying by the scale (one rounding) gives the pair, already in order.
+// kScale = false (channel-wise scales, applied in the epilogue): the exact q.
+template <bool kScale = true>
 __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
   uint32_t h[4];
@@ -201,10 +203,15 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   for (int i = 0; i < 4; ++i) {
     const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
     __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t), k136);
-    __nv_bfloat162 v = __hmul2(q, s2);
-    h[i] = *reinterpret_cast<const uint32_t*>(&v);
+    if (kScale) q = __hmul2(q, s2);
+    h[i] = *reinterpret_cast<const uint32_t*>(&q);
   }
   return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+// Eight values of a packed word: scaled (group scales) or exact q (channel).
+__device__ __forceinline__ uint4 restore_word(uint32_t w, __nv_bfloat162 s2, bool channel) {
+  return channel ? dequant_word<false>(w, s2) : dequant_word<true>(w, s2);
 }
 
 // Group table: s.off <- offsets, s.tile_start <- exclusive scan of tiles per
@@ -289,6 +296,13 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
     tc_fence_after();
     const uint32_t tbase =
         tmem_base + static_cast<uint32_t>(acc * BN_MAX) + (static_cast<uint32_t>(sp * 32) << 16);
+    // Channel-wise W4A16 scales: this lane's accumulator row is weight row
+    // tile_weight_row(32 * sp + lane); its scale multiplies the exact-q sums.
+    float row_scale = 1.0f;
+    if (p.channel) {
+      const uint16_t* sc = t.shared ? p.wscale_s : p.wscale;
+      row_scale = bf16_bits_to_float(__ldg(sc + tile_weight_row(p, t, 32 * sp + lane)));
+    }
     for (int c0 = 0; c0 < t.bn; c0 += 16) {
       uint32_t r[16];
       tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), r);
@@ -301,6 +315,10 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
           r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
       } else {
         tmem_wait_ld();
+      }
+      if (p.channel) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * row_scale);
       }
       if (p.op == kOpGateUp) {
         // lanes 0-15 hold gate rows, lanes 16-31 the up rows of the same 16
@@ -798,7 +816,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           if (kb >= t.k_blocks) continue;
           const int buf = 2 * grp + h;
           const int g = (kb * kBK) / p.group;
-          const uint16_t sbits = table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
+          const uint16_t sbits = p.channel ? uint16_t{0x3F80} : table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
           __nv_bfloat162 s2;
           s2.x = __ushort_as_bfloat16(sbits);
           s2.y = s2.x;
@@ -812,7 +830,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           uint8_t* arow = s.a[buf] + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(words[c], s2);
+            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = restore_word(words[c], s2, p.channel != 0);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&s.aready[buf]);
@@ -1193,7 +1211,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
         for (int h = 0; h < kMyBlocks; ++h) {
           const int j = kSub * h + hd;
           const int g = ((kb0 + j) * kBK) / p.group;
-          const uint16_t sbits = table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
+          const uint16_t sbits = p.channel ? uint16_t{0x3F80} : table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
           __nv_bfloat162 s2;
           s2.x = __ushort_as_bfloat16(sbits);
           s2.y = s2.x;
@@ -1202,7 +1220,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
           uint32_t v[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 d = dequant_word(words[c], s2);
+            const uint4 d = restore_word(words[c], s2, p.channel != 0);
             v[4 * c] = d.x;
             v[4 * c + 1] = d.y;
             v[4 * c + 2] = d.z;

@@ -190,10 +190,12 @@ int validate(const moe_config* c) {
   if (c->quant == MOE_QUANT_BF16) {
     if (c->I % 64 != 0 || c->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
   } else if (c->quant == MOE_QUANT_W4A16) {
-    // symmetric int4, group 128 along K only (other layouts are rejected, as
-    // unsupported quantisation formats are rejected at model load); K tiles of
+    // symmetric int4 with group-128 scales along K or channel-wise scales
+    // (group 0, one per output row); other layouts are rejected, as
+    // unsupported quantisation formats are rejected at model load.  K tiles of
     // 256 packed values: D, I and I_shared multiples of 256
-    if (c->group != 128 || c->D % 256 != 0 || c->I % 256 != 0 || c->I_shared % 256 != 0)
+    if ((c->group != 128 && c->group != 0) || c->D % 256 != 0 || c->I % 256 != 0 ||
+        c->I_shared % 256 != 0)
       return MOE_ERR_UNSUPPORTED;
   } else {
     return MOE_ERR_UNSUPPORTED;
@@ -374,7 +376,10 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   p.wscale_s = static_cast<const uint16_t*>(a->ws_scales);
   p.K = gate_up ? c->D : c->I;
   p.K_s = gate_up ? c->D : c->I_shared;
-  p.group = w4 ? c->group : 128;
+  // channel-wise scales: the restore leaves q unscaled and the epilogue
+  // multiplies each accumulator row by its row's scale
+  p.channel = (w4 && c->group == 0) ? 1 : 0;
+  p.group = (w4 && c->group > 0) ? c->group : 128;
   const int bn_max = choose_bn_max(c);
   // The W4A16 64-row kernel copies token rows in 32-row boxes, the others in 16.
   const uint32_t tok_rows = (w4 && bn_max == 64) ? 32 : 16;
@@ -435,7 +440,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   // up to 4096 (whole rows of 8..32 scales, 16..64 B) and the 64-row variant runs.
   const bool k_ok = p.K % 1024 == 0 && p.K <= 4096 && (!has_shared || (p.K_s % 1024 == 0 &&
                                                                       p.K_s <= 4096));
-  p.scale_table = (w4 && bn_max == 64 && k_ok) ? 1 : 0;
+  p.scale_table = (w4 && !p.channel && bn_max == 64 && k_ok) ? 1 : 0;
   if (p.scale_table) {
     const uint64_t rows_r = gate_up ? 2ull * c->I : static_cast<uint64_t>(c->D);
     ok &= map_scales(&maps.sc, a->w_scales, c->E, rows_r, p.K / c->group, gate_up);

@@ -67,6 +67,7 @@ struct GemmParams {
   int K, K_s;               // reduction sizes (elements)
   int group;
   int scale_table;          // W4A16: tile scales come from tm_sc / tm_sc_s by TMA
+  int channel;              // W4A16: one scale per weight row ([rows]), applied in the epilogue
 };
 
 struct GemmMaps {

@@ -38,7 +38,7 @@ class MoEConfig:
     Is: int         # shared-expert intermediate size
     k: int          # experts per token
     quant: int = 0  # 0 = bf16 weights, 1 = W4A16 (int4 group-quantised)
-    group: int = 128
+    group: int = 128  # W4A16 scale group along K; 0 = channel-wise (one scale per row)
     zipf_s: float = 0.0     # > 0: add a log-Zipf router bias
     zipf_alpha: float = 0.0  # scale of that bias
     seed: int = 0
@@ -71,6 +71,10 @@ CONFIGS = {
     # W4A16 at the decode batch (T=64): ~370 touched experts, 1-6 rows each.
     "w4a16_decode": MoEConfig("w4a16_decode", T=64, D=4096, E=512, I=1024, Is=1024, k=10,
                               quant=1, group=128),
+    # W4A16 with channel-wise scales (one bf16 scale per output row), the release
+    # note's other supported scale strategy, at the prefill batch.
+    "w4a16_channel": MoEConfig("w4a16_channel", T=1024, D=4096, E=512, I=1024, Is=1024, k=10,
+                               quant=1, group=0),
     # Compute-bound grouped GEMM: T=8192 on 64 experts, ~1280 rows per expert
     # (256-row token tiles), where the tensor pipe rather than HBM bounds the GEMMs.
     "dense_e64": MoEConfig("dense_e64", T=8192, D=4096, E=64, I=1024, Is=1024, k=10),
@@ -112,16 +116,19 @@ PACK_SHIFTS = (0, 16, 4, 20, 8, 24, 12, 28)
 
 
 def quantize_w4(w: torch.Tensor, group: int = 128):
-    """Symmetric int4, one bf16 scale per ``group`` consecutive K values.
+    """Symmetric int4, one bf16 scale per ``group`` consecutive K values
+    (group 0: channel-wise, one scale per row).
 
-    w: [..., R, C] bf16.  Returns (q [..., R, C/8] int32, s [..., R, C/group] bf16)
-    with s = bf16(absmax / 7), q = clamp(round_half_even(w / s), -8, 7) (q = 0
-    where s = 0).  Pair order within each int32: value 2i of the group of 8 in
-    bits [4i, 4i+4), value 2i+1 in bits [16+4i, 20+4i).
+    w: [..., R, C] bf16.  Returns (q [..., R, C/8] int32, s [..., R, C/group] bf16,
+    or s [..., R] when group is 0) with s = bf16(absmax / 7),
+    q = clamp(round_half_even(w / s), -8, 7) (q = 0 where s = 0).  Pair order
+    within each int32: value 2i of the group of 8 in bits [4i, 4i+4), value 2i+1
+    in bits [16+4i, 20+4i).
     """
     *lead, R, C = w.shape
-    assert C % group == 0 and C % 8 == 0
-    wf = w.to(torch.float32).reshape(*lead, R, C // group, group)
+    g = C if group == 0 else group
+    assert C % g == 0 and C % 8 == 0
+    wf = w.to(torch.float32).reshape(*lead, R, C // g, g)
     s = (wf.abs().amax(dim=-1) / 7.0).to(torch.bfloat16)
     sf = s.to(torch.float32).unsqueeze(-1)
     safe = torch.where(sf == 0, torch.ones_like(sf), sf)
@@ -132,7 +139,7 @@ def quantize_w4(w: torch.Tensor, group: int = 128):
     packed = torch.zeros((*lead, R, C // 8), dtype=torch.int64, device=w.device)
     packed = (q.to(torch.int64) << shifts.to(torch.int64)).sum(dim=-1)
     packed = torch.where(packed >= 2**31, packed - 2**32, packed).to(torch.int32)
-    return packed, s
+    return packed, (s.squeeze(-1) if group == 0 else s)
 
 
 @dataclass
@@ -188,7 +195,11 @@ def make_inputs(cfg: MoEConfig, device="cpu", weight_device=None) -> MoEInputs:
         s_gu = s_dn = None
     else:
         w_gu, w_dn = alloc((E, 2 * I, D // 8), torch.int32), alloc((E, D, I // 8), torch.int32)
-        s_gu, s_dn = alloc((E, 2 * I, D // G), torch.bfloat16), alloc((E, D, I // G), torch.bfloat16)
+        if G == 0:  # channel-wise: one scale per output row
+            s_gu, s_dn = alloc((E, 2 * I), torch.bfloat16), alloc((E, D), torch.bfloat16)
+        else:
+            s_gu = alloc((E, 2 * I, D // G), torch.bfloat16)
+            s_dn = alloc((E, D, I // G), torch.bfloat16)
     for e in range(E):
         gu, dn = expert_weights_bf16(cfg, e, wdev)
         if cfg.quant == 0:

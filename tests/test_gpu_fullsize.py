@@ -19,7 +19,7 @@ from helpers import WEIGHT_ABS, blob_parts, oracle_layer_rows, oracle_route, tol
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 SAMPLE = {"decode": 64, "prefill": 24, "skewed": 24, "w4a16": 24, "w4a16_decode": 64,
-          "dense_e64": 16}
+          "dense_e64": 16, "w4a16_channel": 24}
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -42,6 +42,13 @@ W4 = {
     "w4_wide": MoEConfig("w4_wide", T=2100, D=256, E=8, I=256, Is=256, k=2, quant=1),
     # K = 1024 / 2048: exercises the TMA scale tables (K multiple of 1024)
     "w4_table": MoEConfig("w4_table", T=96, D=2048, E=12, I=1024, Is=1024, k=3, quant=1),
+    # channel-wise scales (group 0): 64-row kernel (TMEM restore) and 256-row kernel
+    "w4c_ragged": MoEConfig("w4c_ragged", T=37, D=512, E=24, I=768, Is=256, k=3, quant=1,
+                            group=0),
+    "w4c_table": MoEConfig("w4c_table", T=96, D=2048, E=12, I=1024, Is=1024, k=3, quant=1,
+                           group=0),
+    "w4c_wide": MoEConfig("w4c_wide", T=2100, D=256, E=8, I=256, Is=256, k=2, quant=1,
+                          group=0),
 }
 
 
@@ -290,7 +297,8 @@ def test_forward_parity_w4a16(name):
     tol_check(y_host(y), ref)
 
 
-@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide", "w4_table"])
+@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide", "w4_table", "w4c_ragged",
+                                  "w4c_wide"])
 def test_grouped_gate_up_w4a16(name):
     cfg = W4[name]
     host, dev, ids, w, offsets, perm, inv, blob = grouped_setup(cfg)
@@ -316,7 +324,8 @@ def test_grouped_gate_up_w4a16(name):
     tol_check(y_host(hs), ref_s, what="h_shared")
 
 
-@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide", "w4_table"])
+@pytest.mark.parametrize("name", ["w4_tiny", "w4_ragged", "w4_wide", "w4_table", "w4c_ragged",
+                                  "w4c_wide"])
 def test_grouped_down_w4a16(name):
     cfg = W4[name]
     host, dev, ids, w, offsets, perm, inv, blob = grouped_setup(cfg)

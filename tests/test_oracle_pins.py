@@ -394,6 +394,58 @@ def test_w4a16_forward_equals_bf16_forward_on_dequantised_weights():
     assert np.array_equal(y4, yb)
 
 
+def test_dequant_w4_channel_scales():
+    """group 0 (channel-wise): one scale per row, q * s_row exactly."""
+    rng = np.random.default_rng(5)
+    R, C = 5, 48
+    q = rng.integers(-8, 8, size=(R, C))
+    s = bf16_bits(rng.choice([0.5, 0.25, 2.0, 3.0, 0.0078125], size=R))
+    out = oracle.dequant_w4(pack_by_hand(q), s, 0)
+    assert (out == q * u16_to_f64(s)[:, None]).all()
+
+
+def test_w4a16_channel_forward_equals_bf16_forward_on_dequantised_weights():
+    """Channel-wise scales (group 0), power-of-two per row: the W4A16 oracle equals the
+    bf16 oracle on the dequantised weights bit for bit."""
+    T, D, E, I, Is, k = 6, 32, 4, 16, 16, 2
+    rng = np.random.default_rng(3)
+    x = as_u16(normal_bf16((T, D), 1.0, 1, 33))
+    wr = as_u16(normal_bf16((E, D), 0.3, 1, 34))
+
+    def mat(R, C):
+        q = rng.integers(-8, 8, size=(R, C))
+        s = 2.0 ** rng.integers(-6, -2, size=R)
+        return pack_by_hand(q), bf16_bits(s), bf16_bits(q * s[:, None])
+
+    ex_q, ex_b = {}, {}
+    for e in range(E):
+        qg, sg, bg = mat(2 * I, D)
+        qd, sd, bd = mat(D, I)
+        ex_q[e] = (qg, sg, qd, sd)
+        ex_b[e] = (bg, bd)
+    qg, sg, bg = mat(2 * Is, D)
+    qd, sd, bd = mat(D, Is)
+    y4, ids4, _ = oracle.layer(x, wr, k, ex_q, (qg, sg, qd, sd), I=I, Is=Is, quant=1, group=0)
+    yb, idsb, _ = oracle.layer(x, wr, k, ex_b, (bg, bd), I=I, Is=Is, quant=0)
+    assert (ids4 == idsb).all()
+    assert np.array_equal(y4, yb)
+
+
+def test_quantizer_channel_roundtrip_bounds():
+    """Channel-wise quantiser: one scale per row, |w - q s| <= s/2, absmax maps to +-7."""
+    w = normal_bf16((6, 256), 0.05, 0, 43)
+    q, s = quantize_w4(w, 0)
+    assert tuple(s.shape) == (6,)
+    deq = oracle.dequant_w4(q.numpy(), as_u16(s), 0)
+    wf = w.to(torch.float32).numpy().astype(np.float64)
+    sf = u16_to_f64(as_u16(s))[:, None]
+    assert np.all(np.abs(wf - deq) <= sf / 2 * (1 + 1e-12) + 1e-30)
+    codes = np.rint(deq / sf)
+    assert codes.min() >= -8 and codes.max() <= 7
+    am = np.abs(wf).argmax(axis=1)
+    assert all(abs(codes[r, am[r]]) == 7 for r in range(6))
+
+
 def test_quantizer_roundtrip_bounds():
     """Input-side quantiser: codes in [-8, 7], |w - q s| <= s/2, absmax maps to +-7."""
     w = normal_bf16((8, 256), 0.05, 0, 41)
