@@ -62,10 +62,13 @@ def test_invalid_config_rejected_on_host(lib, field, value, code):
     assert rc == code
 
 
-def test_w4a16_group_must_be_128(lib):
+@pytest.mark.parametrize("group,ok", [(128, True), (0, True), (64, False), (256, False),
+                                      (-1, False)])
+def test_w4a16_group_is_128_or_channel(lib, group, ok):
+    """Group scales of 128 along K, or channel-wise (group 0); nothing else."""
     cfg = B.config(CONFIGS["w4a16"])
-    cfg.group = 64
-    assert lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_FORWARD) == 0
+    cfg.group = group
+    assert (lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_FORWARD) > 0) == ok
 
 
 def test_w4a16_needs_whole_packed_k_tiles(lib):
