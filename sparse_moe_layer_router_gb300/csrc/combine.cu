@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
                                                       const float4* __restrict__ o_shared,
                                                       const int32_t* __restrict__ inv_row, int T,
                                                       int D4, int k, uint2* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int c = blockIdx.y * blockDim.x + threadIdx.x;
   if (c >= D4) return;
@@ -43,9 +45,9 @@ void launch_combine(const float* o, const float* o_shared, const int32_t* inv_ro
                     int k, void* y, cudaStream_t st) {
   const int D4 = D / 4;
   dim3 grid(T, (D4 + 255) / 256);
-  combine_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(o),
-                                       reinterpret_cast<const float4*>(o_shared), inv_row, T, D4,
-                                       k, static_cast<uint2*>(y));
+  pdl_launch(combine_kernel, grid, dim3(256), 0, st, reinterpret_cast<const float4*>(o),
+             reinterpret_cast<const float4*>(o_shared), inv_row, T, D4, k,
+             static_cast<uint2*>(y));
 }
 
 // ------------------------------------------------------------------

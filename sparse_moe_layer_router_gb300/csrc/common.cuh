@@ -101,6 +101,18 @@ __device__ __forceinline__ bool mbar_wait_time_only_r(uint64_t* bar, uint32_t pa
   return true;
 }
 
+// ------------------------------------------------------------------ launch chaining
+// Programmatic dependent launch: kernels launched with pdl_launch may start
+// while their predecessor in the stream is still running.  Each kernel first
+// calls pdl_wait (returns once the predecessor grid has completed and its
+// writes are visible; no global memory is touched before it) and then
+// pdl_trigger, which lets its own successor be launched.  The overlap saves
+// the launch latency and the block scheduling of every kernel boundary.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

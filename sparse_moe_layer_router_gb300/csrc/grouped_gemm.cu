@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
                         const __grid_constant__ CUtensorMap tm_b4_s,
                         const __grid_constant__ CUtensorMap tm_b8,
                         const __grid_constant__ CUtensorMap tm_b8_s, const GemmParams p) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   using Smem = Bf16Smem<BN_MAX, STAGES>;
   const uint32_t raw = smem_u32(smem_raw);
@@ -542,6 +543,9 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
     epilogue_role<BN_MAX, 1, true>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
   }
 
+  // The successor may launch once every CTA is past its tiles (a persistent
+  // grid would otherwise let it occupy the SMs' slots for the whole run).
+  pdl_trigger();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -575,6 +579,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
                            const __grid_constant__ CUtensorMap tm_b_s,
                            const __grid_constant__ CUtensorMap tm_sc,
                            const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   using Smem = W4Smem<BN_MAX, PSTAGES, BSTAGES>;
   const uint32_t raw = smem_u32(smem_raw);
@@ -854,6 +859,9 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
   }
 
+  // The successor may launch once every CTA is past its tiles (a persistent
+  // grid would otherwise let it occupy the SMs' slots for the whole run).
+  pdl_trigger();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -925,6 +933,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
                             const __grid_constant__ CUtensorMap tm_b_s,
                             const __grid_constant__ CUtensorMap tm_sc,
                             const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
+  pdl_wait();
   static_assert(ND % 4 == 0 && kKPerPacked % (ND / 4) == 0, "dequant warps per lane quarter");
   constexpr int BN_MAX = 64;
   constexpr int kThreads = w4t_threads<ND>();
@@ -1243,6 +1252,9 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
     if (!ok) record_error(p, abort_flag, MOE_ERR_TIMEOUT);
   }
 
+  // The successor may launch once every CTA is past its tiles (a persistent
+  // grid would otherwise let it occupy the SMs' slots for the whole run).
+  pdl_trigger();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -1259,9 +1271,8 @@ static cudaError_t launch_bf16(const GemmParams& p, const GemmMaps& m, int num_s
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kBaseThreads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.b2, m.b2_s, m.b4, m.b4_s,
-                                             m.b8, m.b8_s, p);
-  return cudaGetLastError();
+  return pdl_launch(kern, dim3(num_sms), dim3(kBaseThreads), smem, st, m.a, m.a_s, m.b, m.b_s,
+                    m.b2, m.b2_s, m.b4, m.b4_s, m.b8, m.b8_s, p);
 }
 
 template <int BN_MAX, int PSTAGES, int BSTAGES>
@@ -1272,8 +1283,8 @@ static cudaError_t launch_w4(const GemmParams& p, const GemmMaps& m, int num_sms
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kW4Threads, smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
-  return cudaGetLastError();
+  return pdl_launch(kern, dim3(num_sms), dim3(kW4Threads), smem, st, m.a, m.a_s, m.b, m.b_s, m.sc,
+                    m.sc_s, p);
 }
 
 template <int PSTAGES, int TSTAGES, int ND>
@@ -1284,8 +1295,8 @@ static cudaError_t launch_w4t(const GemmParams& p, const GemmMaps& m, int num_sm
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, w4t_threads<ND>(), smem, st>>>(m.a, m.a_s, m.b, m.b_s, m.sc, m.sc_s, p);
-  return cudaGetLastError();
+  return pdl_launch(kern, dim3(num_sms), dim3(w4t_threads<ND>()), smem, st, m.a, m.a_s, m.b, m.b_s,
+                    m.sc, m.sc_s, p);
 }
 
 cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int bn_max, int quant,

@@ -546,6 +546,11 @@ int begin(const moe_config* c, int entry, void* ws, size_t ws_bytes, DevInfo* de
 
 }  // namespace
 
+// Chained (programmatic dependent) launches for batches up to 32768 pairs.
+static bool chain_launches(const moe_config* c) {
+  return c && static_cast<long>(c->T) * c->k <= 32768;
+}
+
 extern "C" {
 
 size_t moe_workspace_size(const moe_config* cfg, int entry) {
@@ -556,6 +561,7 @@ size_t moe_workspace_size(const moe_config* cfg, int entry) {
 
 int moe_route(const moe_config* cfg, const void* x, const void* w_router, const float* bias,
               int32_t* blob, void* ws, size_t ws_bytes, void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   if (!x || !w_router || !blob) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(blob) || (bias && !aligned16(bias)))
     return MOE_ERR_ALIGN;
@@ -568,6 +574,7 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_router, const 
 
 int moe_router_logits(const moe_config* cfg, const void* x, const void* w_router, float* z,
                       void* ws, size_t ws_bytes, void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   if (!x || !w_router || !z) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(z)) return MOE_ERR_ALIGN;
   DevInfo dev;
@@ -588,6 +595,7 @@ int moe_router_logits(const moe_config* cfg, const void* x, const void* w_router
 int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int32_t* offsets,
                 int32_t* perm_pair, int32_t* inv_row, const void* x, void* x_perm, void* ws,
                 size_t ws_bytes, void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   if (!blob || !counts || !offsets || !perm_pair || !inv_row) return MOE_ERR_INVALID_ARG;
   if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_ALIGN;
@@ -606,6 +614,7 @@ int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int
 int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* counts,
                        int32_t* offsets, int32_t* perm_pair, int32_t* inv_row, const void* x,
                        void* x_perm, void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   int rc = validate(cfg);
   if (rc) return rc;
   if (!blob || !counts || !offsets || !perm_pair || !inv_row) return MOE_ERR_INVALID_ARG;
@@ -624,6 +633,7 @@ int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* coun
 
 int moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws, size_t ws_bytes,
                      void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   int rc = validate(cfg);
   if (rc) return rc;
   rc = check_gemm_args(cfg, args);
@@ -639,6 +649,7 @@ int moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws,
 
 int moe_combine(const moe_config* cfg, const float* o, const float* o_shared,
                 const int32_t* inv_row, void* y, void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   int rc = validate(cfg);
   if (rc) return rc;
   if (!o || !inv_row || !y) return MOE_ERR_INVALID_ARG;
@@ -653,6 +664,7 @@ int moe_combine(const moe_config* cfg, const float* o, const float* o_shared,
 
 int moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* y, void* ws,
                 size_t ws_bytes, void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   int rc = validate(cfg);
   if (rc) return rc;
   if (!x || !y) return MOE_ERR_INVALID_ARG;
@@ -668,6 +680,7 @@ int moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void
 
 int moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w, void* y_host,
                      void* ws, size_t ws_bytes, void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
   int rc = validate(cfg);
   if (rc) return rc;
   if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;

@@ -9,6 +9,38 @@ namespace moe {
 
 constexpr int kPermuteChunk = 2048;  // pairs per permute block
 
+// ---- chained launches (the kernels call griddepcontrol.wait / .launch_dependents)
+// Whether launches on this host thread are chained (set per call by the entry
+// points: on for batches up to 32768 (token, slot) pairs, where launch latency
+// is a visible share of the step; at larger batches the early-launched grids
+// measured slower).
+inline bool& pdl_enabled() {
+  static thread_local bool on = true;
+  return on;
+}
+struct PdlScope {
+  bool prev;
+  explicit PdlScope(bool on) : prev(pdl_enabled()) { pdl_enabled() = on; }
+  ~PdlScope() { pdl_enabled() = prev; }
+};
+
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+
 // ---- router (router.cu)
 cudaError_t launch_router_logits_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                                     const void* x, const void* wr, int T, int D, int E, int S,

@@ -26,6 +26,8 @@ __device__ __forceinline__ int pair_expert(const int32_t* __restrict__ blob, int
 __global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __restrict__ blob,
                                                             int P, int k, int E,
                                                             int32_t* __restrict__ chunk_cnt) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -43,6 +45,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
                                                             int B, int E,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sums[32];
   __shared__ int carry;
   if (threadIdx.x == 0) carry = 0;
@@ -95,6 +99,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
 __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const int32_t* __restrict__ blob, int P, int k, int E, const int32_t* __restrict__ chunk_base,
     int32_t* __restrict__ perm_pair, int32_t* __restrict__ inv_row) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int wcnt[];  // [8][E]
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) wcnt[i] = 0;
@@ -137,6 +143,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ idx,
                                                           int rows, int vec_per_row, int div,
                                                           uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   if (r >= rows) return;
   const int src = idx[r] / div;
@@ -153,6 +161,8 @@ constexpr int kPermuteOneBlockMaxPairs = 4096;
 __global__ void __launch_bounds__(1024) permute_one_block_kernel(
     const int32_t* __restrict__ blob, int P, int k, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm_pair, int32_t* __restrict__ inv_row) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int wc[];  // [32][E], then [32] warp sums
   int* warp_sums = wc + 32 * E;
   __shared__ int carry;
@@ -234,9 +244,8 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
                                            static_cast<int>(smem_one));
       if (e != cudaSuccess) return e;
     }
-    permute_one_block_kernel<<<1, 1024, smem_one, st>>>(blob, P, k, E, counts, offsets, perm_pair,
-                                                        inv_row);
-    return cudaGetLastError();
+    return pdl_launch(permute_one_block_kernel, dim3(1), dim3(1024), smem_one, st, blob, P, k, E,
+                      counts, offsets, perm_pair, inv_row);
   }
   const int B = (P + kPermuteChunk - 1) / kPermuteChunk;
   const size_t smem_count = static_cast<size_t>(E) * sizeof(int);
@@ -247,17 +256,19 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
                                          static_cast<int>(smem_scatter));
     if (e != cudaSuccess) return e;
   }
-  permute_count_kernel<<<B, 256, smem_count, st>>>(blob, P, k, E, chunk_cnt);
-  permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_cnt, B, E, counts, offsets);
-  permute_scatter_kernel<<<B, 256, smem_scatter, st>>>(blob, P, k, E, chunk_cnt, perm_pair,
-                                                       inv_row);
-  return cudaGetLastError();
+  cudaError_t e = pdl_launch(permute_count_kernel, dim3(B), dim3(256), smem_count, st, blob, P, k,
+                             E, chunk_cnt);
+  if (e != cudaSuccess) return e;
+  e = pdl_launch(permute_scan_kernel, dim3(1), dim3(1024), 0, st, chunk_cnt, B, E, counts, offsets);
+  if (e != cudaSuccess) return e;
+  return pdl_launch(permute_scatter_kernel, dim3(B), dim3(256), smem_scatter, st, blob, P, k, E,
+                    chunk_cnt, perm_pair, inv_row);
 }
 
 void launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div, void* out,
                         cudaStream_t st) {
-  gather_rows_kernel<<<rows, 256, 0, st>>>(static_cast<const uint4*>(a), idx, rows, D / 8, div,
-                                           static_cast<uint4*>(out));
+  pdl_launch(gather_rows_kernel, dim3(rows), dim3(256), 0, st, static_cast<const uint4*>(a), idx,
+             rows, D / 8, div, static_cast<uint4*>(out));
 }
 
 // ------------------------------------------------------------------

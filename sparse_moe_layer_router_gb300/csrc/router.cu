@@ -51,6 +51,8 @@ struct RouterTcSmem {
 __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, int T,
     int E, int nkb, int kbs, float* __restrict__ z_part, int* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   RouterTcSmem& s =
@@ -194,6 +196,8 @@ __global__ void __launch_bounds__(256) router_sumsq_kernel(const __nv_bfloat16* 
                                                            int T, int E, int D,
                                                            float* __restrict__ xsq,
                                                            float* __restrict__ wsq) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= T + E) return;
   const uint4* src = reinterpret_cast<const uint4*>(
@@ -341,6 +345,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     const float* __restrict__ wsq_part, float gamma, const __nv_bfloat16* __restrict__ x,
     const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
     int* __restrict__ counters, float gamma2) {
+  pdl_wait();
+  pdl_trigger();
   // shared: zx double[E] (level-3 logits) | sc float2[E] (level-2 pairs) |
   //         vs float[E] | wss float[E] | clist int[E] | stage uint4[64]
   extern __shared__ double sel_smem[];
@@ -660,6 +666,8 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(
     const float* __restrict__ wsq_part, float gamma, const __nv_bfloat16* __restrict__ x,
     const __nv_bfloat16* __restrict__ wr, int32_t* __restrict__ blob,
     int* __restrict__ counters, float gamma2) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ double zx_smem[];  // [8 warps][E] refined logits, then [8][64] uint4 staging
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + wib;
@@ -931,17 +939,17 @@ cudaError_t launch_router_logits_tc(const CUtensorMap& tm_w, const CUtensorMap& 
                                     const void* x, const void* wr, int T, int D, int E, int S,
                                     int kbs, float* z_part, float* xsq, float* wsq, int* status,
                                     cudaStream_t st) {
-  router_sumsq_kernel<<<(T + E + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                                         static_cast<const __nv_bfloat16*>(wr),
-                                                         T, E, D, xsq, wsq);
+  cudaError_t e = pdl_launch(router_sumsq_kernel, dim3((T + E + 7) / 8), dim3(256), 0, st,
+                             static_cast<const __nv_bfloat16*>(x),
+                             static_cast<const __nv_bfloat16*>(wr), T, E, D, xsq, wsq);
+  if (e != cudaSuccess) return e;
   const size_t smem = sizeof(RouterTcSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((E + kRtE - 1) / kRtE, (T + kRtT - 1) / kRtT, S);
-  router_logits_tc_kernel<<<grid, 192, smem, st>>>(tm_w, tm_x, T, E, D / 64, kbs, z_part, status);
-  return cudaGetLastError();
+  return pdl_launch(router_logits_tc_kernel, grid, dim3(192), smem, st, tm_w, tm_x, T, E, D / 64,
+                    kbs, z_part, status);
 }
 
 cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E, int k,
@@ -965,9 +973,8 @@ cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E
                                             static_cast<int>(smem));                          \
       if (e_ != cudaSuccess) return e_;                                                       \
     }                                                                                         \
-    kern<<<blocks, 256, smem, st>>>(z_part, S, T, D, E, k, bias, xsq_part, wsq_part, gamma,   \
-                                    xb, wb, blob, counters, gamma2);                          \
-    return cudaGetLastError();                                                                \
+    return pdl_launch(kern, dim3(blocks), dim3(256), smem, st, z_part, S, T, D, E, k, bias,  \
+                      xsq_part, wsq_part, gamma, xb, wb, blob, counters, gamma2);             \
   }
   MOE_SELECT_CASE(1)
   MOE_SELECT_CASE(4)
