@@ -122,6 +122,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
+def slowest_rank(x, world, device):
+    """The largest of every rank's ``x`` (a duration): the job runs as long as its
+    slowest replica.  One rank: ``x`` itself."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank_step, steps, seconds):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / seconds
+
+
 def scales_per_row(cfg, K):
     """bf16 scales per weight row of length K: K / group, or 1 (channel-wise, group 0)."""
     return 1 if cfg.group == 0 else K // cfg.group
@@ -350,12 +367,9 @@ def main():
     barrier()
     ms_total = e0.elapsed_time(e1)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = slowest_rank(ms_total, world, dev)
     ms_step = ms_total / args.steps
-    value = world * cfg.T * args.steps / (ms_total / 1e3)
+    value = job_tokens_per_s(world, cfg.T, args.steps, ms_total / 1e3)
     # sums of squares, logits, select, dispatch (one block up to 4096 pairs, else
     # count + scan + scatter), gather, 2 GEMMs, combine
     launches_per_step = 8 if cfg.T * cfg.k <= 4096 else 10
@@ -446,11 +460,8 @@ def main():
             stream.synchronize()  # the step's result is on the host
         barrier()
         dt = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([dt], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * cfg.T * ke / dt, "unit": "tokens/s",
+        dt = slowest_rank(dt, world, dev)
+        e2e = {"value": job_tokens_per_s(world, cfg.T, ke, dt), "unit": "tokens/s",
                "h2d_bytes_per_step": cfg.T * cfg.D * 2, "d2h_bytes_per_step": cfg.T * cfg.D * 2,
                "ms_per_step": 1e3 * dt / ke, "steps": ke,
                "same_output_as_device_path": bool(torch.equal(yh, y.cpu()))}

@@ -1,0 +1,51 @@
+"""The bench's multi-rank arithmetic on CPU: two gloo ranks (127.0.0.1) report
+different durations; both must see the slowest, and the job throughput counts
+every rank's tokens over that time."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        ms = [12.5, 20.0][rank]
+        slow = bench.slowest_rank(ms, world, "cpu")
+        out[rank] = (slow, bench.job_tokens_per_s(world, 64, 10, slow / 1e3))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_and_job_throughput_two_ranks():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0] == res[1]
+    slow, value = res[0]
+    assert slow == 20.0
+    assert value == pytest.approx(2 * 64 * 10 / 0.020)
+
+
+def test_single_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.slowest_rank(3.5, 1, "cpu") == 3.5
+    assert bench.job_tokens_per_s(1, 64, 100, 2.0) == 3200.0
