@@ -153,7 +153,7 @@ def test_router_logits_tensor_core_error_bound():
 @pytest.mark.parametrize("T,E,k", [(100, 1000, 8), (2100, 1024, 8), (2100, 33, 3)])
 def test_route_bit_exact_wide_and_long(T, E, k):
     """Many experts (up to 1024: 32 logits per lane in the select kernels) and batches
-    past 2048 tokens (the warp-per-token select), with a ragged expert count."""
+    of 512 tokens or more (the warp-per-token select), with a ragged expert count."""
     cfg = MoEConfig(f"r{T}x{E}", T=T, D=256, E=E, I=64, Is=64, k=k)
     host, dev = gpu_inputs(cfg)
     check_route(cfg, host, dev)
