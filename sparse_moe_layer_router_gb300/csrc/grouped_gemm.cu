@@ -59,6 +59,10 @@ constexpr int kDequantWarps = kDequantGroups * kWarpsPerGroup;
 constexpr int kTokenWarp = 6 + kDequantWarps;  // W4A16: separate producer for token tiles
 constexpr int kW4Threads = kBaseThreads + 32 * kDequantWarps + 32;
 constexpr int kScaleTabElems = kBM * 32;  // one tile's scales for K <= 4096
+// W4A16 scale group along K.  The host accepts group 128 or channel-wise
+// scales only, so the kernels divide by a constant (a power of two) instead
+// of a run-time value.
+constexpr int kGroup = 128;
 
 struct TileInfo {
   int shared;
@@ -652,7 +656,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
             ok = false;
             break;
           }
-          const int ngrp = (t.shared ? p.K_s : p.K) / p.group;
+          const int ngrp = (t.shared ? p.K_s : p.K) / kGroup;
           const CUtensorMap* msc = t.shared ? &tm_sc_s : &tm_sc;
           mbar_arrive_expect_tx(&s.sfull[sb], static_cast<uint32_t>(kBM * ngrp * 2));
           if (p.op == kOpGateUp) {
@@ -800,7 +804,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
       const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
       const int K = t.shared ? p.K_s : p.K;
-      const int ngrp = K / p.group;
+      const int ngrp = K / kGroup;
       const uint16_t* srow = (t.shared ? p.wscale_s : p.wscale) +
                              static_cast<size_t>(tile_weight_row(p, t, r)) * ngrp;
       const int sb = tile_ctr & 1;
@@ -820,7 +824,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           const int kb = kb0 + j;
           if (kb >= t.k_blocks) continue;
           const int buf = 2 * grp + h;
-          const int g = (kb * kBK) / p.group;
+          const int g = (kb * kBK) / kGroup;
           const uint16_t sbits = p.channel ? uint16_t{0x3F80} : table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
           __nv_bfloat162 s2;
           s2.x = __ushort_as_bfloat16(sbits);
@@ -1020,7 +1024,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
             ok = false;
             break;
           }
-          const int ngrp = (t.shared ? p.K_s : p.K) / p.group;
+          const int ngrp = (t.shared ? p.K_s : p.K) / kGroup;
           const CUtensorMap* msc = t.shared ? &tm_sc_s : &tm_sc;
           if (lane == 0) {
             mbar_arrive_expect_tx(&s.sfull[sb], static_cast<uint32_t>(kBM * ngrp * 2));
@@ -1180,7 +1184,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
     for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
       const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
       const int K = t.shared ? p.K_s : p.K;
-      const int ngrp = K / p.group;
+      const int ngrp = K / kGroup;
       const uint16_t* srow = (t.shared ? p.wscale_s : p.wscale) +
                              static_cast<size_t>(tile_weight_row(p, t, r)) * ngrp;
       const int sb = tile_ctr & 1;
@@ -1219,7 +1223,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
 #pragma unroll
         for (int h = 0; h < kMyBlocks; ++h) {
           const int j = kSub * h + hd;
-          const int g = ((kb0 + j) * kBK) / p.group;
+          const int g = ((kb0 + j) * kBK) / kGroup;
           const uint16_t sbits = p.channel ? uint16_t{0x3F80} : table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
           __nv_bfloat162 s2;
           s2.x = __ushort_as_bfloat16(sbits);
