@@ -22,7 +22,9 @@ using namespace moe;
 // Workspace header: status word (int32 at 0); router counters (int32 at 4:
 // tokens re-decided at level 2, at 8: tokens that needed level 3).
 constexpr size_t kHeader = 256;
-constexpr int kRouterTargetCtas = 304;
+// Router logits: split K until about this many CTAs run (half the SMs: fewer
+// split partials for the select kernel to add; measured best of 76..608).
+constexpr int kRouterTargetCtas = 76;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
