@@ -91,6 +91,19 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
 
 
+def test_router_logits_host_validation(lib):
+    cfg = B.config(CONFIGS["tiny"])
+    d = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4096 + 4)
+    assert lib.moe_router_logits(ctypes.byref(cfg), d, d, None, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_logits(ctypes.byref(cfg), d, d, odd, d, 1 << 30, None) == B.MOE_ERR_ALIGN
+    need = lib.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_ROUTE)
+    assert lib.moe_router_logits(ctypes.byref(cfg), d, d, d, d, need - 1, None) == B.MOE_ERR_WORKSPACE
+    bad = B.config(CONFIGS["tiny"])
+    bad.k = 0
+    assert lib.moe_router_logits(ctypes.byref(bad), d, d, d, d, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+
+
 def test_small_workspace_rejected(lib):
     cfg = B.config(CONFIGS["tiny"])
     d = ctypes.c_void_p(4096)

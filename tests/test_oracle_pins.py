@@ -123,6 +123,20 @@ def test_route_duplicate_router_rows_prefer_lower_index():
     assert D == 4
 
 
+def test_route_single_expert_and_top1():
+    """E = 1: every token goes to expert 0 with weight 1.  k = 1: the argmax, weight 1
+    (renormalising over one selected expert)."""
+    T, D = 4, 8
+    x, wr1 = small_inputs(T, D, 1, 9)
+    ids, w = oracle.route(x, wr1, 1)
+    assert (ids == 0).all() and (w == 1.0).all()
+    x, wr = small_inputs(T, D, 7, 10)
+    ids, w = oracle.route(x, wr, 1)
+    z = np.array([[float(v) for v in row] for row in exact_logits(x, wr)])
+    assert (ids[:, 0] == np.argmax(z, axis=1)).all()
+    assert (w == 1.0).all()
+
+
 def test_route_k_equals_E_is_dense_softmax():
     """k = E: renormalisation is a no-op and w is the softmax over all experts."""
     T, D, E = 6, 8, 5
