@@ -31,6 +31,9 @@ SMALL = {
     "hot": MoEConfig("hot", T=200, D=256, E=16, I=128, Is=128, k=2, zipf_s=1.2, zipf_alpha=3.0),
     # the 256-row token tile variant
     "wide": MoEConfig("wide", T=2100, D=256, E=8, I=64, Is=64, k=2),
+    # top-1 routing (weight 1), and a single routed expert
+    "top1": MoEConfig("top1", T=50, D=256, E=8, I=128, Is=128, k=1),
+    "single_expert": MoEConfig("single_expert", T=20, D=128, E=1, I=64, Is=64, k=1),
 }
 
 # W4A16: symmetric int4 weights, group 128 along K, bf16 scales
