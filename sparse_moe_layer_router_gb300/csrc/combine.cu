@@ -41,13 +41,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   y[static_cast<size_t>(t) * D4 + c] = out;
 }
 
-void launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T, int D,
-                    int k, void* y, cudaStream_t st) {
+cudaError_t launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T,
+                           int D, int k, void* y, cudaStream_t st) {
   const int D4 = D / 4;
   dim3 grid(T, (D4 + 255) / 256);
-  pdl_launch(combine_kernel, grid, dim3(256), 0, st, reinterpret_cast<const float4*>(o),
-             reinterpret_cast<const float4*>(o_shared), inv_row, T, D4, k,
-             static_cast<uint2*>(y));
+  return pdl_launch(combine_kernel, grid, dim3(256), 0, st, reinterpret_cast<const float4*>(o),
+                    reinterpret_cast<const float4*>(o_shared), inv_row, T, D4, k,
+                    static_cast<uint2*>(y));
 }
 
 // ------------------------------------------------------------------

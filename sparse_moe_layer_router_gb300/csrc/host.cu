@@ -358,7 +358,8 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   if (a->a_row_index) {
     if (!gate_up) return MOE_ERR_INVALID_ARG;
     void* xp = xperm_override ? xperm_override : at<void>(ws, L.xperm);
-    launch_gather_rows(a->a, a->a_row_index, P, c->D, 1, xp, st);
+    const int grc = cuda_rc(launch_gather_rows(a->a, a->a_row_index, P, c->D, 1, xp, st));
+    if (grc) return grc;
     b_routed = xp;
   }
   GemmMaps maps;
@@ -502,8 +503,9 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
                               at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), st));
   if (rc) return rc;
   // dispatch: token rows in grouped order (pair index / k = token)
-  launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k, at<void>(ws, L.xperm),
-                     st);
+  rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k,
+                                  at<void>(ws, L.xperm), st));
+  if (rc) return rc;
   moe_gemm_args g{};
   g.op = MOE_OP_GATE_UP_SWIGLU;
   g.a = at<void>(ws, L.xperm);
@@ -532,9 +534,8 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   d.out_shared = at<void>(ws, L.os);
   rc = gemm_impl(c, dev, &d, ws, L, st, nullptr);
   if (rc) return rc;
-  launch_combine(at<float>(ws, L.o), at<float>(ws, L.os), at<int32_t>(ws, L.inv), c->T, c->D,
-                 c->k, y, st);
-  return cuda_rc(cudaGetLastError());
+  return cuda_rc(launch_combine(at<float>(ws, L.o), at<float>(ws, L.os), at<int32_t>(ws, L.inv),
+                                c->T, c->D, c->k, y, st));
 }
 
 int begin(const moe_config* c, int entry, void* ws, size_t ws_bytes, DevInfo* dev, Layout* L) {
@@ -609,8 +610,7 @@ int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int
   rc = cuda_rc(launch_permute(blob, cfg->T, cfg->k, cfg->E, at<int32_t>(ws, L.chunk), counts,
                               offsets, perm_pair, inv_row, st));
   if (rc || !x) return rc;
-  launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, x_perm, st);
-  return cuda_rc(cudaGetLastError());
+  return cuda_rc(launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, x_perm, st));
 }
 
 int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* counts,
@@ -659,9 +659,8 @@ int moe_combine(const moe_config* cfg, const float* o, const float* o_shared,
   DevInfo dev;
   rc = current_device(&dev);
   if (rc) return rc;
-  launch_combine(o, o_shared, inv_row, cfg->T, cfg->D, cfg->k, y,
-                 static_cast<cudaStream_t>(stream));
-  return cuda_rc(cudaGetLastError());
+  return cuda_rc(launch_combine(o, o_shared, inv_row, cfg->T, cfg->D, cfg->k, y,
+                                static_cast<cudaStream_t>(stream)));
 }
 
 int moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* y, void* ws,

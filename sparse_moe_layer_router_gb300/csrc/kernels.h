@@ -55,8 +55,8 @@ cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E
 cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,
                            int32_t* counts, int32_t* offsets, int32_t* perm_pair,
                            int32_t* inv_row, cudaStream_t st);
-void launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div, void* out,
-                        cudaStream_t st);
+cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
+                               void* out, cudaStream_t st);
 // Capacity (int32 entries) of the fixed device array behind moe_permute_static.
 constexpr long kStaticPermuteScratchInts = 65536;
 cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int32_t* counts,
@@ -64,8 +64,8 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
                                   const void* x, int D, void* x_perm, cudaStream_t st);
 
 // ---- combine (combine.cu)
-void launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T, int D,
-                    int k, void* y, cudaStream_t st);
+cudaError_t launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T,
+                           int D, int k, void* y, cudaStream_t st);
 
 // ---- bounded-wait self-test (combine.cu)
 cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st);

@@ -265,10 +265,10 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
                     chunk_cnt, perm_pair, inv_row);
 }
 
-void launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div, void* out,
-                        cudaStream_t st) {
-  pdl_launch(gather_rows_kernel, dim3(rows), dim3(256), 0, st, static_cast<const uint4*>(a), idx,
-             rows, D / 8, div, static_cast<uint4*>(out));
+cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
+                               void* out, cudaStream_t st) {
+  return pdl_launch(gather_rows_kernel, dim3(rows), dim3(256), 0, st,
+                    static_cast<const uint4*>(a), idx, rows, D / 8, div, static_cast<uint4*>(out));
 }
 
 // ------------------------------------------------------------------
@@ -312,8 +312,7 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
   if (e != cudaSuccess) return e;
   e = launch_permute(blob, T, k, E, table, counts, offsets, perm_pair, inv_row, st);
   if (e != cudaSuccess || !x) return e;
-  launch_gather_rows(x, perm_pair, T * k, D, k, x_perm, st);
-  return cudaGetLastError();
+  return launch_gather_rows(x, perm_pair, T * k, D, k, x_perm, st);
 }
 
 }  // namespace moe
