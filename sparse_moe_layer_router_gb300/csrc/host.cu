@@ -93,22 +93,6 @@ bool map_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Gate/up weights [groups][2*half][cols]: 3-D map {cols, groups*2*half rows, 2} whose
-// third axis steps from a gate row to the matching up row (half rows further);
-// box {64, 16, 2} = 16 gate rows followed by the 16 matching up rows.
-bool map_gate_up_bf16(CUtensorMap* m, const void* base, uint64_t groups, uint64_t half,
-                      uint64_t cols) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {cols, groups * 2 * half, 2};
-  const cuuint64_t strides[2] = {cols * 2, half * cols * 2};
-  const cuuint32_t box[3] = {64, 16, 2};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Gate/up weights [groups][2*half][cols] bf16 as a 4-D map {64-element K
 // chunk, 16 rows, gate/up, 16-row block}: one {64, 16, 2, 4} box is a whole
 // 64-feature k-block stage (four blocks of 16 gate rows followed by their 16
@@ -141,8 +125,10 @@ bool map_2d_i4(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Packed int4 gate/up weights [groups][2*half][cols/8]: the 3-D gate/up pairing
-// of map_gate_up_bf16 with a {32 words, 16, 2} box and the 128-byte swizzle.
+// Packed int4 gate/up weights [groups][2*half][cols/8] as a 3-D map {cols/8
+// words, groups*2*half rows, 2} whose third axis steps from a gate row to the
+// matching up row (half rows further): a {32 words, 16, 2} box is 16 gate rows
+// followed by the 16 matching up rows (128-byte swizzle).
 bool map_gate_up_i4(CUtensorMap* m, const void* base, uint64_t groups, uint64_t half,
                     uint64_t cols) {
   EncodeTiledFn enc = encode_fn();
