@@ -13,8 +13,9 @@
 // accumulator per 64-wide K chunk whose fp32 values are then added in order,
 // so |v - z| <= r = gamma * ||x_t|| * ||Wr_e|| + 2^-23 |v| (the Cauchy-Schwarz
 // bound on sum |x_d Wr_ed|; gamma covers the chunk accumulation, the chunk and
-// split sums and the fp64 definition's own deviation).  A token whose k-th / (k+1)-th boundary is
-// separated by these intervals is certified; otherwise the experts whose
+// split sums and the fp64 definition's own deviation).  A token whose k-th /
+// (k+1)-th boundary is separated by these intervals is certified; otherwise
+// the experts whose
 // intervals straddle the boundary are recomputed with a compensated fp32 dot
 // product whose rigorous radius is ~1e-10 of sum |x_d w_d| (level 2), and only
 // if that still cannot separate them with the defining fp64 index-order sum
@@ -656,7 +657,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
   }
 }
 
-// Warp-per-token variant for large T (eight tokens per block): the same
+// Warp-per-token variant for T >= 512 (eight tokens per block): the same
 // decision as router_select_kernel, with the level-2 candidates of a token
 // recomputed one after another by its warp.
 template <int VPL>
