@@ -15,12 +15,11 @@
 // bound on sum |x_d Wr_ed|; gamma covers the chunk accumulation, the chunk and
 // split sums and the fp64 definition's own deviation).  A token whose k-th /
 // (k+1)-th boundary is separated by these intervals is certified; otherwise
-// the experts whose
-// intervals straddle the boundary are recomputed with a compensated fp32 dot
-// product whose rigorous radius is ~1e-10 of sum |x_d w_d| (level 2), and only
-// if that still cannot separate them with the defining fp64 index-order sum
-// itself (level 3: exact ties).  The result equals the definition's decision
-// (ties: lower index).
+// the experts whose intervals straddle the boundary are recomputed with a
+// compensated fp32 dot product whose rigorous radius is ~1e-10 of
+// sum |x_d w_d| (level 2), and only if that still cannot separate them with
+// the defining fp64 index-order sum itself (level 3: exact ties).  The result
+// equals the definition's decision (ties: lower index).
 #include "common.cuh"
 #include "kernels.h"
 
