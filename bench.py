@@ -1,4 +1,5 @@
-"""Benchmark of the MoE layer forward (decode step: T=64, D=4096, E=512, I=1024, top-10).
+"""Benchmark of the MoE layer forward: decode step (T=64, D=4096, E=512, I=1024,
+top-10) as the headline, and the T=1024 prefill chunk beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -15,6 +16,12 @@ expert included) over one batch of synthetic input, through the C ABI.
             launch / its mean CUDA-event duration inside a timed pass of the
             path split into its ABI calls, against the measured HBM copy peak.
   cpu_baseline  the fp64 oracle on this host's cores over the same batch.
+  configs.prefill  the same measurements for the T=1024 prefill chunk on the
+            same expert weights (the metric's second configuration).
+
+After warm-up, after the timed steps, after the split pass and after the e2e
+steps the workspace status words are read: a kernel that recorded a device
+error (a bounded wait that gave up) fails the run instead of being timed.
 
 With --gpus N > 1 (launched by torch.distributed.run) every rank runs an
 independent replica of the layer on its own GPU (the path has no exchange step
@@ -28,7 +35,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -39,7 +45,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (T=64 decode, T=1024 prefill) and % of HBM/BF16 roofline"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "grouped_gemm_gate_up_decode.md")
+# ncu DRAM counters of the decode gate/up launch with the hash of the kernel
+# sources they were taken with (machine-readable; the .md beside it explains them)
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "grouped_gemm_gate_up_decode.json")
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e nominal (context for the measured-copy fraction)
 GEMM_SOURCES = [os.path.join(ROOT, "sparse_moe_layer_router_gb300", "csrc", f)
                 for f in ("grouped_gemm.cu", "common.cuh")]
 L2_BYTES = 129 * 2**20
@@ -55,6 +64,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="with the default decode workload, skip the T=1024 prefill line")
     return ap.parse_args()
 
 
@@ -145,7 +156,9 @@ def scales_per_row(cfg, K):
 
 
 def touched_gate_up_bytes(cfg, counts):
-    """Algorithmic HBM bytes of one grouped gate/up launch (see DESIGN)."""
+    """Algorithmic HBM bytes of one grouped gate/up launch: every touched expert's
+    gate/up weights (and scales) once, the shared expert's, the token rows read
+    and the hidden rows written."""
     import torch
     touched = int((counts > 0).sum().item())
     P = cfg.T * cfg.k
@@ -177,22 +190,23 @@ def layer_bytes_flops(cfg, touched):
     return byts, flops
 
 
+def gate_up_flops(cfg):
+    """Tensor-core flops of one grouped gate/up launch (routed pairs + shared rows)."""
+    return 2 * cfg.T * cfg.k * cfg.D * 2 * cfg.I + 2 * cfg.T * cfg.D * 2 * cfg.Is
+
+
 def profile_traffic():
-    """(traffic bytes per launch, ncu workload scale note) from the committed ncu summary,
-    or (None, why) when the kernel sources changed since the counters were taken."""
-    if not os.path.exists(PROFILE_SUMMARY):
-        return None, "no committed ncu summary"
-    txt = open(PROFILE_SUMMARY).read()
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
-    if not (m_sha and m_tr):
-        return None, "summary lacks traffic"
+    """(traffic bytes per decode gate/up launch, source) from the committed ncu
+    counters, or (None, why) when the kernel sources changed since they were taken."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None, "no committed ncu counters"
+    d = json.load(open(PROFILE_TRAFFIC))
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
         h.update(open(f, "rb").read())
-    if h.hexdigest() != m_sha.group(1):
+    if h.hexdigest() != d.get("source_sha256"):
         return None, "kernel changed since the ncu capture"
-    return int(m_tr.group(1)), "ncu"
+    return int(d["traffic_bytes_per_launch"]), "ncu"
 
 
 def peaks():
@@ -299,43 +313,26 @@ def run_reference(args, cfg, base_config, local):
                     "d2h_bytes_per_step": 0}}
 
 
-# ------------------------------------------------------------------ main
-def main():
-    args = parse()
+# ------------------------------------------------------------------ GPU leg
+class DeviceError(RuntimeError):
+    pass
+
+
+def check_status(B, ws, what):
+    """Fail the run if a kernel recorded a device-side error (a wait that gave
+    up stops issuing work, so its step would be timed as if it had run)."""
+    st = B.get_status(ws)
+    if st != B.MOE_OK:
+        raise DeviceError(f"device status {st} ({B.strerror(st)}) after {what}")
+
+
+def measure(cfg, inp, args, world, rank, dev, clocks_on, hbm_peak, bf16_peak, peak_src,
+            with_traffic):
+    """One workload: K timed moe_forward steps, the path split into its ABI calls
+    (per-call CUDA events), e2e through moe_forward_host, and the oracle baseline."""
     import torch
-    import torch.distributed as dist
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
-
     from sparse_moe_layer_router_gb300 import binding as B
-    from sparse_moe_layer_router_gb300.build import build
-    from sparse_moe_layer_router_gb300.synthetic import CONFIGS, make_inputs
 
-    cfg = CONFIGS[args.config]
-    hbm_peak, bf16_peak, peak_src = peaks()
-    base_config = {"workload": workload_desc(cfg), "T": cfg.T, "D": cfg.D, "E": cfg.E,
-                   "I": cfg.I, "Is": cfg.Is, "k": cfg.k, "quant": cfg.quant,
-                   "parallelism": f"replicas x{args.gpus}",
-                   "l2": "no flush: the touched expert weights streamed each step exceed L2 (129 MB)",
-                   "seed": cfg.seed}
-
-    if args.impl == "reference":
-        if rank == 0:
-            line = run_reference(args, cfg, base_config, local)
-            print(json.dumps(line), flush=True)
-        if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
-        return
-
-    torch.cuda.set_device(local)
-    build()
-    dev = torch.device("cuda", local)
-    inp = make_inputs(cfg, device=dev)
     stream = torch.cuda.current_stream()
     ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD, dev)
     y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=dev)
@@ -347,17 +344,16 @@ def main():
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    status = B.get_status(ws)
-    if status != B.MOE_OK:
-        raise RuntimeError(f"device status {status} after warm-up")
+    check_status(B, ws, "warm-up")
 
     def barrier():
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize()
 
     # ---------------- timed region: K steps of moe_forward
-    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    clocks = ClockSampler(dev.index, enabled=clocks_on)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -367,6 +363,7 @@ def main():
     barrier()
     ms_total = e0.elapsed_time(e1)
     clk = clocks.stop()
+    check_status(B, ws, "the timed steps")
     ms_total = slowest_rank(ms_total, world, dev)
     ms_step = ms_total / args.steps
     value = job_tokens_per_s(world, cfg.T, args.steps, ms_total / 1e3)
@@ -417,19 +414,26 @@ def main():
     for i in range(ksplit):
         split_step(evs[i])
     barrier()
+    for w_, what in ((ws_r, "route"), (ws_p, "permute"), (ws_g, "the grouped GEMMs")):
+        check_status(B, w_, f"the split pass ({what})")
     per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(ksplit)) / ksplit
            for j, n in enumerate(names)}
     split_total = sum(evs[i][0].elapsed_time(evs[i][5]) for i in range(ksplit)) / ksplit
     same = bool(torch.equal(y, y2))
+    refined = int(ws_r[4:8].view(torch.int32).item())
+    exact = int(ws_r[8:12].view(torch.int32).item())
 
     counts = perm_out[0]
     gu_bytes, touched = touched_gate_up_bytes(cfg, counts)
     gu_ms = per["gate_up"]
     achieved = gu_bytes / (gu_ms / 1e3) / 1e9
-    traffic, traffic_src = profile_traffic()
+    gu_tflops = gate_up_flops(cfg) / (gu_ms / 1e3) / 1e12
+    traffic, traffic_src = profile_traffic() if with_traffic else (None, "not captured")
     roofline = {"bound": "hbm", "kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_source": f"{peak_src} (HBM copy, burst)",
+                "frac_of_nominal_hbm": achieved / NOMINAL_HBM_GBS,
+                "tensor_tflops": gu_tflops, "tensor_frac": gu_tflops / bf16_peak,
                 "traffic": traffic, "traffic_source": traffic_src,
                 "algorithmic_bytes_per_launch": gu_bytes, "touched_experts": touched,
                 "mean_launch_ms": gu_ms}
@@ -440,8 +444,8 @@ def main():
              "binding_frac": max(lay_bytes / (hbm_peak * 1e9), lay_flops / (bf16_peak * 1e12))
              / (ms_step / 1e3),
              "per_call_ms": per, "split_step_ms": split_total, "split_matches_forward": same,
-             "router_refined_tokens": int(ws[4:8].view(torch.int32).item()),
-             "router_exact_fallback_tokens": int(ws[8:12].view(torch.int32).item())}
+             "router_refined_tokens": refined, "router_exact_fallback_tokens": exact}
+    del xp, h, hs, o, os_, ws_r, ws_p, ws_g
 
     # ---------------- e2e: host buffers through moe_forward_host
     e2e = None
@@ -460,11 +464,13 @@ def main():
             stream.synchronize()  # the step's result is on the host
         barrier()
         dt = time.perf_counter() - t0
+        check_status(B, ws_h, "the e2e steps")
         dt = slowest_rank(dt, world, dev)
         e2e = {"value": job_tokens_per_s(world, cfg.T, ke, dt), "unit": "tokens/s",
                "h2d_bytes_per_step": cfg.T * cfg.D * 2, "d2h_bytes_per_step": cfg.T * cfg.D * 2,
                "ms_per_step": 1e3 * dt / ke, "steps": ke,
                "same_output_as_device_path": bool(torch.equal(yh, y.cpu()))}
+        del ws_h
 
     # ---------------- CPU baseline: the oracle on this host's cores (rank 0 only, N = 1)
     cpu = None
@@ -476,15 +482,73 @@ def main():
         cpu = {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"the full {cfg.name} batch ({cfg.T} tokens; fp64 routing + layer) "
                          f"x{passes} passes"}
+        del inputs
+    del ws, y
+    return {"value": value, "ms_per_step": ms_step, "roofline": roofline, "layer": layer,
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+            "gpu_launches": launches_per_step * args.steps, "workload": workload_desc(cfg)}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse()
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+
+    from sparse_moe_layer_router_gb300.build import build
+    from sparse_moe_layer_router_gb300.synthetic import CONFIGS, make_inputs, with_tokens
+
+    cfg = CONFIGS[args.config]
+    hbm_peak, bf16_peak, peak_src = peaks()
+    base_config = {"workload": workload_desc(cfg), "T": cfg.T, "D": cfg.D, "E": cfg.E,
+                   "I": cfg.I, "Is": cfg.Is, "k": cfg.k, "quant": cfg.quant,
+                   "parallelism": f"replicas x{args.gpus}",
+                   "l2": "no flush: the touched expert weights streamed each step exceed L2 (129 MB)",
+                   "seed": cfg.seed}
+
+    if args.impl == "reference":
+        if rank == 0:
+            line = run_reference(args, cfg, base_config, local)
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    build()
+    dev = torch.device("cuda", local)
+    inp = make_inputs(cfg, device=dev)
+    head = measure(cfg, inp, args, world, rank, dev, not args.no_clocks, hbm_peak, bf16_peak,
+                   peak_src, with_traffic=args.config == "decode")
+    extra = {}
+    if args.config == "decode" and not args.decode_only:
+        # the metric's second configuration: the T=1024 prefill chunk on the same
+        # expert weights (only the token rows differ)
+        pre = with_tokens(inp, CONFIGS["prefill"])
+        r = measure(pre.cfg, pre, args, world, rank, dev, not args.no_clocks, hbm_peak,
+                    bf16_peak, peak_src, with_traffic=False)
+        extra["prefill"] = {"metric": METRIC, "unit": "tokens/s", "steps": args.steps,
+                            "config": {"workload": r.pop("workload"), "T": pre.cfg.T}, **r}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-                "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(3, args.warmup),
+                "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded; random-init weights of the stated shapes)",
-                "config": base_config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches_per_step * args.steps, "clocks": clk, "layer": layer,
-                "impl": "gb300"}
+                "config": base_config, "roofline": head["roofline"],
+                "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
+                "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+                "layer": head["layer"], "impl": "gb300"}
+        if extra:
+            line["configs"] = extra
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

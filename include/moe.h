@@ -64,11 +64,16 @@ extern "C" {
 
 /* ---- weight formats ---- */
 #define MOE_QUANT_BF16 0    /* bf16 expert weights                                   */
-#define MOE_QUANT_W4A16 1   /* symmetric int4, 8 per int32 in pair order (value 2i
+#define MOE_QUANT_W4A16 1   /* symmetric int4, 8 per int32 in PAIR order (value 2i
                                in bits 4i..4i+3, value 2i+1 in bits 16+4i..19+4i,
                                two's complement); bf16 scales, one per `group` = 128
                                K values ([rows][K/128]) or, with group = 0, one per
-                               output row ([rows], channel-wise) [R1] */
+                               output row ([rows], channel-wise) [R1].
+                               The pair order is this library's storage layout: it
+                               is NOT the sequential nibble order of the
+                               pack-quantized checkpoint format [R1] (value j in
+                               bits 4j..4j+3).  Convert sequential words once, when
+                               the weights are loaded, with moe_repack_int4. */
 
 /* ---- grouped GEMM operations ---- */
 #define MOE_OP_GATE_UP_SWIGLU 0  /* h = silu(a.Wg^T) * (a.Wu^T) -> bf16               */
@@ -80,6 +85,11 @@ extern "C" {
 #define MOE_ENTRY_GROUPED_GEMM 2
 #define MOE_ENTRY_FORWARD 3
 #define MOE_ENTRY_FORWARD_HOST 4
+#define MOE_ENTRY_FORWARD_EXPERTS 5
+
+/* ---- source layouts of packed int4 words (moe_repack_int4) ---- */
+#define MOE_INT4_SEQUENTIAL 0          /* value j in bits 4j..4j+3, two's complement */
+#define MOE_INT4_SEQUENTIAL_OFFSET8 1  /* value j in bits 4j..4j+3, stored as q + 8  */
 
 /*
  * Shapes of one layer call.
@@ -151,7 +161,10 @@ typedef struct moe_gemm_args {
 
 /*
  * Workspace bytes an entry needs for `cfg` (0 on invalid config).  The first
- * 256 bytes of every workspace are a status header read by moe_get_status.
+ * 256 bytes of every workspace are a status header read by moe_get_status:
+ * zero them once when the workspace is created (the status word is then
+ * written only by a kernel that records an error, and cleared only by
+ * moe_get_status).
  */
 size_t moe_workspace_size(const moe_config *cfg, int entry);
 
@@ -216,8 +229,10 @@ int moe_permute(const moe_config *cfg, const int32_t *blob, int32_t *counts,
  *   Same arguments and results as moe_permute, bit for bit, without ws.
  *   Limit: ceil(T*k / 2048) * E <= 65536 (e.g. E = 512: T*k <= 262144);
  *   larger problems return MOE_ERR_SCRATCH_LIMIT and launch nothing.
- *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
+ *   The array's device address belongs to the CUDA context: the first call
+ *   in a context (the primary context of a device, or one made current with
+ *   cuCtxCreate / after a reset) looks it up with that context current and
+ *   caches it by the context's unique ID; make that first call before any
  *   stream capture.
  *   All calls share the one array: calls that may overlap on the GPU (other
  *   streams, other host threads) race and must be serialised by the caller.
@@ -245,8 +260,12 @@ int moe_combine(const moe_config *cfg, const float *o, const float *o_shared,
                 const int32_t *inv_row, void *y, void *stream);
 
 /*
- * Whole layer: route -> permute -> grouped gate/up (+shared) -> grouped down
- * (+shared) -> combine.  x bf16 [T][D], y bf16 [T][D].
+ * Whole layer [P1, P3, P3B, PM]: route (softmax over E, top-k, renormalised,
+ * packed blob) -> permute (dispatch by expert) -> grouped gate/up + SiLU.mul
+ * (routed experts and the always-on shared expert) -> grouped down with the
+ * routing weight -> combine (unpermute, sum, one bf16 rounding).
+ *   x bf16 [T][D], y bf16 [T][D]; ws sized for MOE_ENTRY_FORWARD.
+ * Errors: as the per-stage calls; nothing is launched on a host-side error.
  */
 int moe_forward(const moe_config *cfg, const void *x, const moe_weights *w,
                 void *y, void *ws, size_t ws_bytes, void *stream);
@@ -261,9 +280,63 @@ int moe_forward_host(const moe_config *cfg, const void *x_host,
                      size_t ws_bytes, void *stream);
 
 /*
- * Device status of the last calls that used `ws`: synchronises `stream`,
- * returns MOE_OK or the first device-side error recorded (MOE_ERR_TIMEOUT
- * when a bounded wait inside a kernel gave up), then clears it.
+ * Expert-parallel slice of the layer [P3B, P3]: the part of the layer output
+ * that one device of an expert-parallel group computes when it holds only the
+ * routed experts [e_begin, e_end) ("Systems engineering playbook: optimizing
+ * Qwen 3.5-397B MoE on Ironwood (TPU7x)", section 3, "Option B": every device
+ * receives all tokens and the packed routing blob, filters the (token, slot)
+ * pairs routed to its own experts, computes them, and the outputs are
+ * reduce-scattered back to the devices that own the tokens; "3-to-2
+ * All-Gather": ids and weights travel as the one int32 blob of moe_route).
+ *   y_partial fp32 [T][D] = sum over slots j with e_begin <= ids[t][j] < e_end
+ *                           of w[t][j] * FFN_{ids[t][j]}(x_t)
+ *                         + FFN_shared(x_t) for shared_begin <= t < shared_end.
+ * Summing y_partial over a partition of [0, E) whose parts give the shared
+ * expert disjoint token ranges covering [0, T), and rounding once to bf16,
+ * gives the layer output of moe_forward (up to the fp32 summation order).
+ *   cfg       T = tokens in x and blob (all devices' tokens), E = ALL experts.
+ *   x         bf16 [T][D];  blob int32 [T][2][k] as written by moe_route.
+ *   w         routed weights of the LOCAL experts only: w_gate_up / w_down (and
+ *             W4A16 scales) hold e_end - e_begin experts, local expert i being
+ *             global expert e_begin + i; w_router and router_bias are unused
+ *             (may be NULL); shared weights are needed when
+ *             shared_end > shared_begin.
+ *   0 <= e_begin < e_end <= E; 0 <= shared_begin <= shared_end <= T.
+ *   ws sized for MOE_ENTRY_FORWARD_EXPERTS.
+ * Errors: MOE_ERR_INVALID_ARG for a bad range or a missing pointer; otherwise
+ * as moe_forward.  Expert ids in the blob outside [0, E) are undefined input.
+ */
+int moe_forward_experts(const moe_config *cfg, const void *x, const int32_t *blob,
+                        const moe_weights *w, int e_begin, int e_end, int shared_begin,
+                        int shared_end, float *y_partial, void *ws, size_t ws_bytes,
+                        void *stream);
+
+/*
+ * Load-time conversion of packed int4 weights to this library's pair order
+ * (MOE_QUANT_W4A16) [R1] ("vLLM TPU Inference v0.31.0: hierarchical MoE
+ * dispatch and W4A16", 4-bit weight section: symmetric int4 weights in the
+ * pack-quantized format, 8 values per int32).
+ *   src       int32 [n_words], eight 4-bit values per word in sequential order
+ *             (value j in bits 4j..4j+3, j = 0..7), as two's complement
+ *             (MOE_INT4_SEQUENTIAL) or offset binary q + 8
+ *             (MOE_INT4_SEQUENTIAL_OFFSET8);
+ *   dst       int32 [n_words] in pair order (value 2i in bits 4i..4i+3, value
+ *             2i+1 in bits 16+4i..19+4i), two's complement.  dst == src (in
+ *             place) is allowed; otherwise the ranges must not overlap.
+ * Bit-exact.  Both pointers are device pointers, 16-byte aligned.  Scales are
+ * not touched.  MOE_ERR_INVALID_ARG for a null pointer or an unknown layout.
+ */
+int moe_repack_int4(const int32_t *src, int32_t *dst, size_t n_words, int src_layout,
+                    void *stream);
+
+/*
+ * Device status of the calls that used `ws` since the status was last read:
+ * synchronises `stream`, returns MOE_OK or the first device-side error
+ * recorded (MOE_ERR_TIMEOUT when a bounded wait inside a kernel gave up), then
+ * clears it.  The status is sticky: no other entry point clears it, so an
+ * error recorded by one call is still reported after later calls succeed.  A
+ * kernel that records an error stops issuing work, so any output written by a
+ * call since the last MOE_OK status is not to be trusted.
  */
 int moe_get_status(void *ws, void *stream);
 

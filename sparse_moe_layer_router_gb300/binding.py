@@ -34,10 +34,14 @@ MOE_ENTRY_PERMUTE = 1
 MOE_ENTRY_GROUPED_GEMM = 2
 MOE_ENTRY_FORWARD = 3
 MOE_ENTRY_FORWARD_HOST = 4
+MOE_ENTRY_FORWARD_EXPERTS = 5
+MOE_INT4_SEQUENTIAL = 0
+MOE_INT4_SEQUENTIAL_OFFSET8 = 1
 
 # Every function declared in include/moe.h.
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_router_logits", "moe_permute", "moe_permute_static",
-           "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status",
+           "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host",
+           "moe_forward_experts", "moe_repack_int4", "moe_get_status",
            "moe_selftest_wait_timeout", "moe_strerror")
 
 
@@ -90,12 +94,16 @@ def lib():
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
             L.moe_forward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
             L.moe_forward_host.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, S, P]
+            L.moe_forward_experts.argtypes = [cfgp, P, P, ctypes.POINTER(MoeWeights), I, I, I, I,
+                                              P, P, S, P]
+            L.moe_repack_int4.argtypes = [P, P, S, I, P]
             L.moe_get_status.argtypes = [P, P]
             L.moe_selftest_wait_timeout.argtypes = [P, S, ctypes.c_uint, P]
             L.moe_strerror.argtypes = [I]
             L.moe_strerror.restype = ctypes.c_char_p
-            for n in ("moe_route", "moe_router_logits", "moe_permute", "moe_permute_static", "moe_grouped_gemm",
-                      "moe_combine", "moe_forward", "moe_forward_host", "moe_get_status",
+            for n in ("moe_route", "moe_router_logits", "moe_permute", "moe_permute_static",
+                      "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host",
+                      "moe_forward_experts", "moe_repack_int4", "moe_get_status",
                       "moe_selftest_wait_timeout"):
                 getattr(L, n).restype = I
             _lib = L
@@ -255,12 +263,41 @@ def forward_host(cfg, x_host, weights, y_host, ws, stream=None):
     return y_host
 
 
+def forward_experts(cfg, x, blob, weights, e_begin, e_end, shared_begin=0, shared_end=0,
+                    y_partial=None, ws=None, stream=None):
+    """fp32 [T, D] partial output of the routed experts [e_begin, e_end) (``weights``
+    holds those experts only) plus the shared expert on tokens [shared_begin, shared_end)."""
+    if not isinstance(weights, MoeWeights):
+        weights = weights_struct(weights)
+    if y_partial is None:
+        y_partial = torch.empty((cfg.T, cfg.D), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(cfg, MOE_ENTRY_FORWARD_EXPERTS, x.device)
+    _check(lib().moe_forward_experts(ctypes.byref(config(cfg)), _p(x), _p(blob),
+                                     ctypes.byref(weights), int(e_begin), int(e_end),
+                                     int(shared_begin), int(shared_end), _p(y_partial), _p(ws),
+                                     ws.numel(), _stream(stream)), "moe_forward_experts")
+    return y_partial
+
+
+def repack_int4(src, dst=None, layout=MOE_INT4_SEQUENTIAL, stream=None):
+    """Sequential-order packed int4 words (int32 tensor) -> this library's pair order."""
+    if src.dtype != torch.int32:
+        raise ValueError("packed int4 words are int32")
+    if dst is None:
+        dst = torch.empty_like(src)
+    _check(lib().moe_repack_int4(_p(src), _p(dst), src.numel(), int(layout), _stream(stream)),
+           "moe_repack_int4")
+    return dst
+
+
 def get_status(ws, stream=None) -> int:
     return int(lib().moe_get_status(_p(ws), _stream(stream)))
 
 
-def selftest_wait_timeout(ws, limit_ms=200, stream=None) -> int:
-    """Run the bounded-wait self-test; returns the device status it leaves (MOE_ERR_TIMEOUT)."""
+def selftest_wait_timeout(ws, limit_ms=200, stream=None, read_status=True):
+    """Run the bounded-wait self-test; returns the device status it leaves
+    (MOE_ERR_TIMEOUT), or None with ``read_status=False`` (status left unread)."""
     _check(lib().moe_selftest_wait_timeout(_p(ws), ws.numel(), int(limit_ms), _stream(stream)),
            "moe_selftest_wait_timeout")
-    return get_status(ws, stream)
+    return get_status(ws, stream) if read_status else None

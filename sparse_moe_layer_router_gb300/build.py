@@ -20,7 +20,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["host.cu", "router.cu", "permute.cu", "grouped_gemm.cu", "combine.cu"]
+SOURCES = ["host.cu", "router.cu", "permute.cu", "grouped_gemm.cu", "combine.cu", "repack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -50,6 +50,48 @@ cudaError_t launch_combine(const float* o, const float* o_shared, const int32_t*
                     static_cast<uint2*>(y));
 }
 
+// Expert-parallel slice ("Option B": each device sums the outputs of its own
+// experts; the devices' fp32 partials are then reduce-scattered):
+//   y32[t][d] = (s0 <= t < s1 ? o_shared[t - s0][d] : 0)
+//             + sum_{j<k, lo <= inv_row[t*k+j] < hi} o[inv_row[t*k+j]][d]
+// with lo, hi read from the device (the local experts' grouped-row range).
+__global__ void __launch_bounds__(256) combine_partial_kernel(
+    const float4* __restrict__ o, const float4* __restrict__ o_shared,
+    const int32_t* __restrict__ inv_row, int T, int D4, int k, const int32_t* __restrict__ row_lo,
+    const int32_t* __restrict__ row_hi, int s0, int s1, float4* __restrict__ y32) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c >= D4) return;
+  const int lo = __ldg(row_lo), hi = __ldg(row_hi);
+  float4 acc = (o_shared && t >= s0 && t < s1)
+                   ? __ldg(o_shared + static_cast<size_t>(t - s0) * D4 + c)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int32_t* rows = inv_row + static_cast<size_t>(t) * k;
+  for (int j = 0; j < k; ++j) {
+    const int r = __ldg(rows + j);
+    if (r < lo || r >= hi) continue;
+    const float4 v = __ldg(o + static_cast<size_t>(r) * D4 + c);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  y32[static_cast<size_t>(t) * D4 + c] = acc;
+}
+
+cudaError_t launch_combine_partial(const float* o, const float* o_shared, const int32_t* inv_row,
+                                   int T, int D, int k, const int32_t* row_lo,
+                                   const int32_t* row_hi, int s0, int s1, float* y32,
+                                   cudaStream_t st) {
+  const int D4 = D / 4;
+  dim3 grid(T, (D4 + 255) / 256);
+  return pdl_launch(combine_partial_kernel, grid, dim3(256), 0, st,
+                    reinterpret_cast<const float4*>(o), reinterpret_cast<const float4*>(o_shared),
+                    inv_row, T, D4, k, row_lo, row_hi, s0, s1, reinterpret_cast<float4*>(y32));
+}
+
 // ------------------------------------------------------------------
 // Self-test of the bounded-wait path every pipelined kernel relies on: one CTA
 // holds TMEM, waits on an mbarrier that nothing arrives on, gives up after

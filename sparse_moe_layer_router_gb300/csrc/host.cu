@@ -251,6 +251,18 @@ Layout layout(const moe_config* c, int entry) {
     case MOE_ENTRY_GROUPED_GEMM:
       L.xperm = cv.take(P * D * 2);  // gathered activation rows when a_row_index is given
       break;
+    case MOE_ENTRY_FORWARD_EXPERTS:
+      L.chunk = cv.take(chunks * E * 4);
+      L.counts = cv.take(E * 4);
+      L.offsets = cv.take((E + 1) * 4);
+      L.perm = cv.take(P * 4);
+      L.inv = cv.take(P * 4);
+      L.xperm = cv.take(P * D * 2);
+      L.h = cv.take(P * I * 2);
+      L.hs = cv.take(T * Is * 2);
+      L.o = cv.take(P * D * 4);
+      L.os = cv.take(T * D * 4);
+      break;
     case MOE_ENTRY_FORWARD:
     case MOE_ENTRY_FORWARD_HOST:
       L.blob = cv.take(T * 2 * k * 4);
@@ -312,8 +324,10 @@ float router_gamma2(const moe_config* c) {
 int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* wr,
                const float* bias, int32_t* blob, void* ws, const Layout& L, cudaStream_t st) {
   const RouterPlan rp = router_plan(c);
-  // Clears the status word and the two refinement counters for this call.
-  if (cudaMemsetAsync(ws, 0, 12, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // Clears the two refinement counters for this call.  The status word before
+  // them is left alone: an error recorded by an earlier call stays until
+  // moe_get_status reads it.
+  if (cudaMemsetAsync(static_cast<char*>(ws) + 4, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
   float* zpart = at<float>(ws, L.zpart);
   float* xsq = at<float>(ws, L.xnorm);
   float* wsq = at<float>(ws, L.wnorm);
@@ -334,8 +348,12 @@ int choose_bn_max(const moe_config* c) {
   return (c->T >= 2048 || avg >= 48.0) ? 256 : 64;
 }
 
+// One grouped GEMM launch over `n_groups` routed groups (a->offsets holds
+// n_groups + 1 row offsets; a->w holds n_groups experts) plus, when
+// a->a_shared is set, a shared group of `t_shared` rows.
 int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, void* ws,
-              const Layout& L, cudaStream_t st, void* xperm_override) {
+              const Layout& L, cudaStream_t st, void* xperm_override, int n_groups,
+              int t_shared) {
   const int P = c->T * c->k;
   const bool gate_up = a->op == MOE_OP_GATE_UP_SWIGLU;
   const bool has_shared = a->a_shared != nullptr;
@@ -344,16 +362,17 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   if (a->a_row_index) {
     if (!gate_up) return MOE_ERR_INVALID_ARG;
     void* xp = xperm_override ? xperm_override : at<void>(ws, L.xperm);
-    const int grc = cuda_rc(launch_gather_rows(a->a, a->a_row_index, P, c->D, 1, xp, st));
+    const int grc =
+        cuda_rc(launch_gather_rows(a->a, a->a_row_index, P, c->D, 1, xp, nullptr, nullptr, st));
     if (grc) return grc;
     b_routed = xp;
   }
   GemmMaps maps;
   GemmParams p{};
   p.op = gate_up ? kOpGateUp : kOpDown;
-  p.E = c->E;
+  p.E = n_groups;
   p.has_shared = has_shared ? 1 : 0;
-  p.T_shared = c->T;
+  p.T_shared = t_shared;
   p.offsets = a->offsets;
   p.perm_pair = a->perm_pair;
   p.blob = a->blob;
@@ -380,8 +399,8 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     p.a_rows_per_expert = 2 * c->I;
     p.ld_out = c->I;
     p.ld_out_s = c->I_shared;
-    ok &= w4 ? map_gate_up_i4(&maps.a, a->w, c->E, c->I, c->D)
-             : map_gate_up_bf16_4d(&maps.a, a->w, c->E, c->I, c->D);
+    ok &= w4 ? map_gate_up_i4(&maps.a, a->w, n_groups, c->I, c->D)
+             : map_gate_up_bf16_4d(&maps.a, a->w, n_groups, c->I, c->D);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, tok_rows);
     if (!w4) {
       ok &= map_2d_bf16(&maps.b2, b_routed, P, c->D, 32);
@@ -391,11 +410,11 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     if (has_shared) {
       ok &= w4 ? map_gate_up_i4(&maps.a_s, a->w_shared, 1, c->I_shared, c->D)
                : map_gate_up_bf16_4d(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
-      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->D, tok_rows);
+      ok &= map_2d_bf16(&maps.b_s, a->a_shared, t_shared, c->D, tok_rows);
       if (!w4) {
-        ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->D, 32);
-        ok &= map_2d_bf16(&maps.b4_s, a->a_shared, c->T, c->D, 64);
-        ok &= map_2d_bf16(&maps.b8_s, a->a_shared, c->T, c->D, 128);
+        ok &= map_2d_bf16(&maps.b2_s, a->a_shared, t_shared, c->D, 32);
+        ok &= map_2d_bf16(&maps.b4_s, a->a_shared, t_shared, c->D, 64);
+        ok &= map_2d_bf16(&maps.b8_s, a->a_shared, t_shared, c->D, 128);
       }
     }
   } else {
@@ -406,8 +425,8 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     p.a_rows_per_expert = c->D;
     p.ld_out = c->D;
     p.ld_out_s = c->D;
-    ok &= w4 ? map_2d_i4(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128)
-             : map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(c->E) * c->D, c->I, 128);
+    ok &= w4 ? map_2d_i4(&maps.a, a->w, static_cast<uint64_t>(n_groups) * c->D, c->I, 128)
+             : map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(n_groups) * c->D, c->I, 128);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, tok_rows);
     if (!w4) {
       ok &= map_2d_bf16(&maps.b2, b_routed, P, c->I, 32);
@@ -417,11 +436,11 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     if (has_shared) {
       ok &= w4 ? map_2d_i4(&maps.a_s, a->w_shared, c->D, c->I_shared, 128)
                : map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
-      ok &= map_2d_bf16(&maps.b_s, a->a_shared, c->T, c->I_shared, tok_rows);
+      ok &= map_2d_bf16(&maps.b_s, a->a_shared, t_shared, c->I_shared, tok_rows);
       if (!w4) {
-        ok &= map_2d_bf16(&maps.b2_s, a->a_shared, c->T, c->I_shared, 32);
-        ok &= map_2d_bf16(&maps.b4_s, a->a_shared, c->T, c->I_shared, 64);
-        ok &= map_2d_bf16(&maps.b8_s, a->a_shared, c->T, c->I_shared, 128);
+        ok &= map_2d_bf16(&maps.b2_s, a->a_shared, t_shared, c->I_shared, 32);
+        ok &= map_2d_bf16(&maps.b4_s, a->a_shared, t_shared, c->I_shared, 64);
+        ok &= map_2d_bf16(&maps.b8_s, a->a_shared, t_shared, c->I_shared, 128);
       }
     }
   }
@@ -432,7 +451,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   p.scale_table = (w4 && !p.channel && bn_max == 64 && k_ok) ? 1 : 0;
   if (p.scale_table) {
     const uint64_t rows_r = gate_up ? 2ull * c->I : static_cast<uint64_t>(c->D);
-    ok &= map_scales(&maps.sc, a->w_scales, c->E, rows_r, p.K / c->group, gate_up);
+    ok &= map_scales(&maps.sc, a->w_scales, n_groups, rows_r, p.K / c->group, gate_up);
     if (has_shared) {
       const uint64_t rows_s = gate_up ? 2ull * c->I_shared : static_cast<uint64_t>(c->D);
       ok &= map_scales(&maps.sc_s, a->ws_scales, 1, rows_s, p.K_s / c->group, gate_up);
@@ -490,7 +509,7 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   if (rc) return rc;
   // dispatch: token rows in grouped order (pair index / k = token)
   rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k,
-                                  at<void>(ws, L.xperm), st));
+                                  at<void>(ws, L.xperm), nullptr, nullptr, st));
   if (rc) return rc;
   moe_gemm_args g{};
   g.op = MOE_OP_GATE_UP_SWIGLU;
@@ -503,7 +522,7 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   g.w_shared = w->ws_gate_up;
   g.ws_scales = w->ss_gate_up;
   g.out_shared = at<void>(ws, L.hs);
-  rc = gemm_impl(c, dev, &g, ws, L, st, nullptr);
+  rc = gemm_impl(c, dev, &g, ws, L, st, nullptr, c->E, c->T);
   if (rc) return rc;
   moe_gemm_args d{};
   d.op = MOE_OP_DOWN_WEIGHTED;
@@ -518,10 +537,66 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   d.w_shared = w->ws_down;
   d.ws_scales = w->ss_down;
   d.out_shared = at<void>(ws, L.os);
-  rc = gemm_impl(c, dev, &d, ws, L, st, nullptr);
+  rc = gemm_impl(c, dev, &d, ws, L, st, nullptr, c->E, c->T);
   if (rc) return rc;
   return cuda_rc(launch_combine(at<float>(ws, L.o), at<float>(ws, L.os), at<int32_t>(ws, L.inv),
                                 c->T, c->D, c->k, y, st));
+}
+
+// Expert-parallel slice: dispatch every pair, but gather, compute and combine
+// only the rows of experts [e0, e1) (local weights indexed e - e0) and the
+// shared expert for tokens [s0, s1).
+int forward_experts_impl(const moe_config* c, const DevInfo& dev, const void* x,
+                         const int32_t* blob, const moe_weights* w, int e0, int e1, int s0, int s1,
+                         float* y32, void* ws, const Layout& L, cudaStream_t st) {
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int rc = cuda_rc(launch_permute(blob, c->T, c->k, c->E, at<int32_t>(ws, L.chunk),
+                                  at<int32_t>(ws, L.counts), offsets, at<int32_t>(ws, L.perm),
+                                  at<int32_t>(ws, L.inv), st));
+  if (rc) return rc;
+  // grouped rows of the local experts: [offsets[e0], offsets[e1])
+  const int32_t* row_lo = offsets + e0;
+  const int32_t* row_hi = offsets + e1;
+  rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k,
+                                  at<void>(ws, L.xperm), row_lo, row_hi, st));
+  if (rc) return rc;
+  const int ts = s1 - s0;
+  const void* x_sh = static_cast<const char*>(x) + static_cast<size_t>(s0) * c->D * 2;
+  moe_gemm_args g{};
+  g.op = MOE_OP_GATE_UP_SWIGLU;
+  g.a = at<void>(ws, L.xperm);
+  g.offsets = offsets + e0;
+  g.w = w->w_gate_up;
+  g.w_scales = w->s_gate_up;
+  g.out = at<void>(ws, L.h);
+  if (ts > 0) {
+    g.a_shared = x_sh;
+    g.w_shared = w->ws_gate_up;
+    g.ws_scales = w->ss_gate_up;
+    g.out_shared = at<void>(ws, L.hs);
+  }
+  rc = gemm_impl(c, dev, &g, ws, L, st, nullptr, e1 - e0, ts);
+  if (rc) return rc;
+  moe_gemm_args d{};
+  d.op = MOE_OP_DOWN_WEIGHTED;
+  d.a = at<void>(ws, L.h);
+  d.offsets = offsets + e0;
+  d.w = w->w_down;
+  d.w_scales = w->s_down;
+  d.perm_pair = at<int32_t>(ws, L.perm);
+  d.blob = blob;
+  d.out = at<void>(ws, L.o);
+  if (ts > 0) {
+    d.a_shared = at<void>(ws, L.hs);
+    d.w_shared = w->ws_down;
+    d.ws_scales = w->ss_down;
+    d.out_shared = at<void>(ws, L.os);
+  }
+  rc = gemm_impl(c, dev, &d, ws, L, st, nullptr, e1 - e0, ts);
+  if (rc) return rc;
+  return cuda_rc(launch_combine_partial(at<float>(ws, L.o), ts > 0 ? at<float>(ws, L.os) : nullptr,
+                                        at<int32_t>(ws, L.inv), c->T, c->D, c->k, row_lo, row_hi,
+                                        s0, s1, y32, st));
 }
 
 int begin(const moe_config* c, int entry, void* ws, size_t ws_bytes, DevInfo* dev, Layout* L) {
@@ -544,7 +619,7 @@ extern "C" {
 
 size_t moe_workspace_size(const moe_config* cfg, int entry) {
   if (validate(cfg) != MOE_OK) return 0;
-  if (entry < MOE_ENTRY_ROUTE || entry > MOE_ENTRY_FORWARD_HOST) return 0;
+  if (entry < MOE_ENTRY_ROUTE || entry > MOE_ENTRY_FORWARD_EXPERTS) return 0;
   return layout(cfg, entry).total;
 }
 
@@ -571,7 +646,6 @@ int moe_router_logits(const moe_config* cfg, const void* x, const void* w_router
   int rc = begin(cfg, MOE_ENTRY_ROUTE, ws, ws_bytes, &dev, &L);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, 12, st) != cudaSuccess) return MOE_ERR_CUDA;
   CUtensorMap mw, mx;
   if (!map_2d_bf16(&mw, w_router, cfg->E, cfg->D, 128) || !map_2d_bf16(&mx, x, cfg->T, cfg->D, 64))
     return MOE_ERR_CUDA;
@@ -596,7 +670,8 @@ int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int
   rc = cuda_rc(launch_permute(blob, cfg->T, cfg->k, cfg->E, at<int32_t>(ws, L.chunk), counts,
                               offsets, perm_pair, inv_row, st));
   if (rc || !x) return rc;
-  return cuda_rc(launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, x_perm, st));
+  return cuda_rc(
+      launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, x_perm, nullptr, nullptr, st));
 }
 
 int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* counts,
@@ -630,9 +705,8 @@ int moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws,
   Layout L;
   rc = begin(cfg, MOE_ENTRY_GROUPED_GEMM, ws, ws_bytes, &dev, &L);
   if (rc) return rc;
-  if (cudaMemsetAsync(ws, 0, 8, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return gemm_impl(cfg, dev, args, ws, L, static_cast<cudaStream_t>(stream), nullptr);
+  return gemm_impl(cfg, dev, args, ws, L, static_cast<cudaStream_t>(stream), nullptr, cfg->E,
+                   cfg->T);
 }
 
 int moe_combine(const moe_config* cfg, const float* o, const float* o_shared,
@@ -690,6 +764,53 @@ int moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weight
   return MOE_OK;
 }
 
+int moe_forward_experts(const moe_config* cfg, const void* x, const int32_t* blob,
+                        const moe_weights* w, int e_begin, int e_end, int shared_begin,
+                        int shared_end, float* y_partial, void* ws, size_t ws_bytes,
+                        void* stream) {
+  PdlScope pdl_scope(chain_launches(cfg));
+  int rc = validate(cfg);
+  if (rc) return rc;
+  if (!x || !blob || !w || !y_partial) return MOE_ERR_INVALID_ARG;
+  if (e_begin < 0 || e_begin >= e_end || e_end > cfg->E) return MOE_ERR_INVALID_ARG;
+  if (shared_begin < 0 || shared_begin > shared_end || shared_end > cfg->T)
+    return MOE_ERR_INVALID_ARG;
+  const bool sh = shared_end > shared_begin;
+  if (!w->w_gate_up || !w->w_down || (sh && (!w->ws_gate_up || !w->ws_down)))
+    return MOE_ERR_INVALID_ARG;
+  const bool w4 = cfg->quant == MOE_QUANT_W4A16;
+  if (w4 && (!w->s_gate_up || !w->s_down || (sh && (!w->ss_gate_up || !w->ss_down))))
+    return MOE_ERR_INVALID_ARG;
+  if (!w4 && (w->s_gate_up || w->s_down || w->ss_gate_up || w->ss_down))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, blob, y_partial, w->w_gate_up, w->w_down, w->s_gate_up, w->s_down,
+                        w->ws_gate_up, w->ws_down, w->ss_gate_up, w->ss_down};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return MOE_ERR_ALIGN;
+  DevInfo dev;
+  Layout L;
+  rc = begin(cfg, MOE_ENTRY_FORWARD_EXPERTS, ws, ws_bytes, &dev, &L);
+  if (rc) return rc;
+  return forward_experts_impl(cfg, dev, x, blob, w, e_begin, e_end, shared_begin, shared_end,
+                              y_partial, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+int moe_repack_int4(const int32_t* src, int32_t* dst, size_t n_words, int src_layout,
+                    void* stream) {
+  if (!src || !dst) return MOE_ERR_INVALID_ARG;
+  if (src_layout != MOE_INT4_SEQUENTIAL && src_layout != MOE_INT4_SEQUENTIAL_OFFSET8)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_ALIGN;
+  if (n_words == 0) return MOE_OK;
+  DevInfo dev;
+  const int rc = current_device(&dev);
+  if (rc) return rc;
+  return cuda_rc(launch_repack_int4(reinterpret_cast<const uint32_t*>(src),
+                                    reinterpret_cast<uint32_t*>(dst), n_words,
+                                    src_layout == MOE_INT4_SEQUENTIAL_OFFSET8,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 int moe_get_status(void* ws, void* stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -709,7 +830,6 @@ int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned int limit_ms, 
   int rc = current_device(&dev);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_rc(launch_selftest_wait(at<int>(ws, 0), 1000000ull * limit_ms, st));
 }
 

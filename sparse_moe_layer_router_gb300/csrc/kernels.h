@@ -55,8 +55,11 @@ cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E
 cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,
                            int32_t* counts, int32_t* offsets, int32_t* perm_pair,
                            int32_t* inv_row, cudaStream_t st);
+// out[r] = a[idx[r] / div] for every row r, or (row_lo, row_hi non-NULL: device
+// pointers to two row indices) only for *row_lo <= r < *row_hi.
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
-                               void* out, cudaStream_t st);
+                               void* out, const int32_t* row_lo, const int32_t* row_hi,
+                               cudaStream_t st);
 // Capacity (int32 entries) of the fixed device array behind moe_permute_static.
 constexpr long kStaticPermuteScratchInts = 65536;
 cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int32_t* counts,
@@ -66,6 +69,17 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
 // ---- combine (combine.cu)
 cudaError_t launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T,
                            int D, int k, void* y, cudaStream_t st);
+
+// Expert-parallel slice: y32[t] = (s0 <= t < s1 ? o_shared[t - s0] : 0)
+//   + sum_j (*row_lo <= inv_row[t*k+j] < *row_hi ? o[inv_row[t*k+j]] : 0), fp32 out.
+cudaError_t launch_combine_partial(const float* o, const float* o_shared, const int32_t* inv_row,
+                                   int T, int D, int k, const int32_t* row_lo,
+                                   const int32_t* row_hi, int s0, int s1, float* y32,
+                                   cudaStream_t st);
+
+// ---- int4 weight layout conversion (repack.cu)
+cudaError_t launch_repack_int4(const uint32_t* src, uint32_t* dst, size_t n_words, bool offset8,
+                               cudaStream_t st);
 
 // ---- bounded-wait self-test (combine.cu)
 cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st);

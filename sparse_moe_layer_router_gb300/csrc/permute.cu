@@ -138,15 +138,19 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
   }
 }
 
-// out[r][:] = a[idx[r] / div][:]  (D bf16 per row, 16-byte vectors).
+// out[r][:] = a[idx[r] / div][:]  (D bf16 per row, 16-byte vectors); with a
+// row range (device pointers row_lo, row_hi) only for *row_lo <= r < *row_hi.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ a,
                                                           const int32_t* __restrict__ idx,
                                                           int rows, int vec_per_row, int div,
-                                                          uint4* __restrict__ out) {
+                                                          uint4* __restrict__ out,
+                                                          const int32_t* __restrict__ row_lo,
+                                                          const int32_t* __restrict__ row_hi) {
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.x;
   if (r >= rows) return;
+  if (row_lo && (r < __ldg(row_lo) || r >= __ldg(row_hi))) return;
   const int src = idx[r] / div;
   const uint4* s = a + static_cast<size_t>(src) * vec_per_row;
   uint4* d = out + static_cast<size_t>(r) * vec_per_row;
@@ -266,41 +270,98 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
 }
 
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
-                               void* out, cudaStream_t st) {
+                               void* out, const int32_t* row_lo, const int32_t* row_hi,
+                               cudaStream_t st) {
   return pdl_launch(gather_rows_kernel, dim3(rows), dim3(256), 0, st,
-                    static_cast<const uint4*>(a), idx, rows, D / 8, div, static_cast<uint4*>(out));
+                    static_cast<const uint4*>(a), idx, rows, D / 8, div, static_cast<uint4*>(out),
+                    row_lo, row_hi);
 }
 
 // ------------------------------------------------------------------
 // Fixed scratch for moe_permute_static: the [chunks][E] count table lives in
 // this file-scope device array (kStaticPermuteScratchInts int32 = 256 KiB)
-// instead of a caller-provided workspace.  Every device that loads the
-// library holds it until the process exits.  Each call overwrites the entries
-// it uses before reading them, so nothing needs clearing; calls that overlap
-// on the GPU share the array and race.
+// instead of a caller-provided workspace.  Every device (every context) that
+// loads the library holds it until the process exits.  Each call overwrites
+// the entries it uses before reading them, so nothing needs clearing; calls
+// that overlap on the GPU share the array and race.
 static __device__ __align__(256) int32_t g_permute_scratch[kStaticPermuteScratchInts];
 
 namespace {
+// The device address of g_permute_scratch belongs to a CUDA context, not to a
+// device: a reset primary context or another context made current on the same
+// device (cuCtxCreate) has its own copy of the array at another address.  The
+// address is therefore cached per context, keyed by the context's unique ID
+// (cuCtxGetId: never reused within the process, unlike a context handle).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  int32_t* addr;
+};
+constexpr int kScratchCache = 32;
 std::mutex g_scratch_mu;
-int32_t* g_scratch_addr[64] = {};
+ScratchEntry g_scratch_cache[kScratchCache] = {};
+int g_scratch_used = 0, g_scratch_next = 0;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+template <typename Fn>
+bool driver_fn(const char* name, Fn* out) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  *out = reinterpret_cast<Fn>(fn);
+  return true;
+}
+
+// ID of the context current on this thread, binding the runtime's primary
+// context first if none is current.  Called with g_scratch_mu held.
+cudaError_t current_ctx_id(unsigned long long* id) {
+  if (!g_ctx_get_current && (!driver_fn("cuCtxGetCurrent", &g_ctx_get_current) ||
+                             !driver_fn("cuCtxGetId", &g_ctx_get_id)))
+    return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (!ctx) {
+    // no context yet: a runtime call that needs one binds the primary context
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (e != cudaSuccess) return e;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorUnknown;
+  }
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
 }  // namespace
 
-// Device address of g_permute_scratch on the current device.  In host code the
-// symbol names a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// Device address of g_permute_scratch in the current context.  In host code
+// the symbol names a host-side stand-in, so the address is looked up with the
+// runtime (once per context, with that context current) and cached.
 static cudaError_t static_scratch(int32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  unsigned long long id = 0;
+  cudaError_t e = current_ctx_id(&id);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < g_scratch_used; ++i)
+    if (g_scratch_cache[i].ctx_id == id) {
+      *out = g_scratch_cache[i].addr;
+      return cudaSuccess;
+    }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_permute_scratch);
+  if (e != cudaSuccess) return e;
+  int i = 0;
+  if (g_scratch_used < kScratchCache) {
+    i = g_scratch_used++;
+  } else {  // full: replace the oldest entry
+    i = g_scratch_next;
+    g_scratch_next = (g_scratch_next + 1) % kScratchCache;
   }
-  *out = g_scratch_addr[dev];
+  ScratchEntry& slot = g_scratch_cache[i];
+  slot.ctx_id = id;
+  slot.addr = static_cast<int32_t*>(p);
+  *out = slot.addr;
   return cudaSuccess;
 }
 
@@ -312,7 +373,7 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
   if (e != cudaSuccess) return e;
   e = launch_permute(blob, T, k, E, table, counts, offsets, perm_pair, inv_row, st);
   if (e != cudaSuccess || !x) return e;
-  return launch_gather_rows(x, perm_pair, T * k, D, k, x_perm, st);
+  return launch_gather_rows(x, perm_pair, T * k, D, k, x_perm, nullptr, nullptr, st);
 }
 
 }  // namespace moe

@@ -226,9 +226,30 @@ __global__ void __launch_bounds__(256) router_sumsq_kernel(const __nv_bfloat16* 
 // ---------------------------------------------------------------- select
 // Upper bound of a Euclidean norm from an fp32 sum of squares: each square
 // passes through at most D/32 + 5 roundings (router_sumsq_kernel), relative
-// error below 2^-9 for D <= 65536; sqrt and the products add 2^-20 of slack.
+// error below 2^-9 for D <= 65536.  A rounding whose result falls below the
+// normal range (2^-126) is off by up to 2^-150 in absolute terms instead, and
+// there are at most D + 32 of them, below 2^-133 in total for D <= 65536.
+// sqrt and the products add 2^-20 of slack.
 __device__ __forceinline__ float norm_bound(float sumsq) {
-  return sqrtf(sumsq * (1.0f + 0x1p-9f)) * (1.0f + 0x1p-20f);
+  return sqrtf(fmaf(sumsq, 1.0f + 0x1p-9f, 0x1p-133f)) * (1.0f + 0x1p-20f);
+}
+
+// Absolute part of the level-1 radius.  The tensor core may flush to zero an
+// input, a product or a partial sum below the fp32 normal range: a lost
+// product with a subnormal input is below 2^-126 times the other operand, a
+// lost product of normal inputs or a lost partial sum below 2^-126, and there
+// are at most D products and D partial sums per logit, so the loss is below
+// 2^-126 (2D + sum_d |x_d| + sum_d |w_d|) <= 2^-126 (2D + sqrt(D) (|x| + |w|));
+// a factor of 4 of slack on top.
+__device__ __forceinline__ float tiny_radius1(int D, float xn, float wn) {
+  return 0x1p-124f * (2.0f * static_cast<float>(D) + sqrtf(static_cast<float>(D)) * (xn + wn));
+}
+
+// Absolute part of the level-2 radius: level 2 forms every product and sum in
+// fp32 on the CUDA cores with subnormals kept, so a result below 2^-126 is off
+// by at most 2^-150, and a logit takes at most D + 64 such roundings.
+__device__ __forceinline__ float tiny_radius2(int D) {
+  return 0x1p-148f * static_cast<float>(D + 64);
 }
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -238,7 +259,8 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 }
 
 // Level 2: compensated fp32 dot product of a token row and a router row (+ bias),
-// warp-cooperative.  Products of two bf16 are exact in fp32; every addition is
+// warp-cooperative.  Products of two bf16 are exact in fp32 down to the normal
+// range (below it, tiny_radius2 covers their rounding); every addition is
 // an error-free TwoSum whose error term is collected in `c`; lanes combine
 // (sum, error) pairs with TwoSum in a butterfly, so every lane ends with the
 // same value.  |(s + c) - exact| <= gamma2 * sum|x_d w_d|, with
@@ -312,12 +334,13 @@ __device__ double warp_exact_logit(const __nv_bfloat16* __restrict__ xr,
         const uint32_t ww[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          // the fp32 product of two bf16 is exact, so adding it in fp64 is the
-          // definition's step
-          acc += static_cast<double>(__uint_as_float(xw[j] << 16) *
-                                     __uint_as_float(ww[j] << 16));
-          acc += static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u) *
-                                     __uint_as_float(ww[j] & 0xFFFF0000u));
+          // the product of two bf16 widened to fp64 is exact over the whole
+          // bf16 range (16 significant bits, exponents within fp64's range),
+          // so adding it in fp64 is the definition's step
+          acc += static_cast<double>(__uint_as_float(xw[j] << 16)) *
+                 static_cast<double>(__uint_as_float(ww[j] << 16));
+          acc += static_cast<double>(__uint_as_float(xw[j] & 0xFFFF0000u)) *
+                 static_cast<double>(__uint_as_float(ww[j] & 0xFFFF0000u));
         }
       }
     }
@@ -407,7 +430,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     if (e < E) {
       wn[i] = norm_bound(wss[e]);
       v[i] = vs[e] + (bias ? __ldg(bias + e) : 0.f);
-      r[i] = gamma * xn * wn[i] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]);
+      r[i] = gamma * xn * wn[i] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]) +
+             tiny_radius1(D, xn, wn[i]);
     } else {
       wn[i] = 0.f;
       v[i] = -INFINITY;
@@ -530,7 +554,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
         const float a = xn * wn[i] + (bias ? fabsf(bias[e]) : 0.f);
         // gamma2 * sum|x w| (level-2 error, plus the fp64 definition's own
         // distance from the exact sum) + rounding of rel and of rel -/+ rad
-        rad[i] = gamma2 * a * (1.0f + 0x1p-20f) + 0x1p-21f * fabsf(rel[i]);
+        rad[i] = gamma2 * a * (1.0f + 0x1p-20f) + 0x1p-21f * fabsf(rel[i]) + tiny_radius2(D);
       }
     }
     uint32_t chosen = 0;
@@ -704,7 +728,8 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(
     wn[i] = norm_bound(wn[i]);
     if (e < E) {
       if (bias) v[i] += __ldg(bias + e);
-      r[i] = gamma * xn * wn[i] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]);
+      r[i] = gamma * xn * wn[i] * (1.0f + 0x1p-10f) + 0x1p-23f * fabsf(v[i]) +
+             tiny_radius1(D, xn, wn[i]);
     } else {
       v[i] = -INFINITY;
       r[i] = 0.f;
@@ -807,7 +832,7 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(
         const float a = xn * wn[i] + (bias ? fabsf(bias[e]) : 0.f);
         // gamma2 * sum|x w| (level-2 error, plus the fp64 definition's own
         // distance from the exact sum) + rounding of rel and of rel -/+ rad
-        rad[i] = gamma2 * a * (1.0f + 0x1p-20f) + 0x1p-21f * fabsf(rel[i]);
+        rad[i] = gamma2 * a * (1.0f + 0x1p-20f) + 0x1p-21f * fabsf(rel[i]) + tiny_radius2(D);
       }
     }
     uint32_t chosen = 0;

@@ -174,6 +174,21 @@ def expert_weights_bf16(cfg: MoEConfig, e: int, device="cpu"):
     return gu, dn
 
 
+def tokens(cfg: MoEConfig, device="cpu") -> torch.Tensor:
+    """The batch's token rows x: bf16 [T, D] ~ N(0, 1), drawn on the CPU."""
+    return normal_bf16((cfg.T, cfg.D), 1.0, cfg.seed, _TAG_X, "cpu").to(device)
+
+
+def with_tokens(inp: MoEInputs, cfg: MoEConfig) -> MoEInputs:
+    """Inputs of ``cfg``, a configuration that differs from ``inp.cfg`` only in
+    the token count T: the same router and expert weights (the expert weights
+    depend on (seed, E, D, I, Is, quant, group) only), fresh token rows."""
+    same = ("D", "E", "I", "Is", "k", "quant", "group", "zipf_s", "zipf_alpha", "seed")
+    if any(getattr(cfg, f) != getattr(inp.cfg, f) for f in same):
+        raise ValueError(f"{cfg.name} differs from {inp.cfg.name} in more than T")
+    return replace(inp, cfg=cfg, x=tokens(cfg, inp.x.device))
+
+
 def make_inputs(cfg: MoEConfig, device="cpu", weight_device=None) -> MoEInputs:
     """All inputs of one layer call.
 
@@ -182,7 +197,7 @@ def make_inputs(cfg: MoEConfig, device="cpu", weight_device=None) -> MoEInputs:
     (default: ``device``), one expert at a time.
     """
     wdev = torch.device(weight_device if weight_device is not None else device)
-    x = normal_bf16((cfg.T, cfg.D), 1.0, cfg.seed, _TAG_X, "cpu")
+    x = tokens(cfg)
     wr = normal_bf16((cfg.E, cfg.D), 0.02, cfg.seed, _TAG_WR, "cpu")
     bias = zipf_bias(cfg.E, cfg.zipf_s, cfg.zipf_alpha, cfg.seed) if cfg.zipf_s > 0 else None
 

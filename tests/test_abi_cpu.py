@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_exports_every_declared_function(lib):
@@ -35,7 +35,7 @@ def test_exports_every_declared_function(lib):
 
 def test_workspace_sizes(lib):
     for name, cfg in CONFIGS.items():
-        for entry in range(5):
+        for entry in range(6):
             n = B.workspace_size(cfg, entry)
             assert n >= 256 and n % 256 == 0, (name, entry, n)
         fwd = B.workspace_size(cfg, B.MOE_ENTRY_FORWARD)
@@ -122,3 +122,26 @@ def test_strerror(lib):
     for c in (0, -1, -2, -3, -4, -5, -6):
         assert B.strerror(c) and B.strerror(c) != "unknown error"
     assert B.strerror(-99) == "unknown error"
+
+
+def test_repack_and_expert_slice_host_validation(lib):
+    d = ctypes.c_void_p(4096)
+    assert lib.moe_repack_int4(None, d, 8, B.MOE_INT4_SEQUENTIAL, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_repack_int4(d, d, 8, 5, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_repack_int4(ctypes.c_void_p(4100), d, 8, 0, None) == B.MOE_ERR_ALIGN
+    assert lib.moe_repack_int4(d, d, 0, 0, None) == B.MOE_OK  # nothing to do
+    cfg = B.config(CONFIGS["tiny"])
+    w = B.MoeWeights(None, None, d, d, None, None, d, d, None, None)
+    ws_n = B.workspace_size(CONFIGS["tiny"], B.MOE_ENTRY_FORWARD_EXPERTS)
+    assert ws_n >= 256
+
+    def call(e0, e1, s0, s1, ws_bytes=ws_n, weights=w):
+        return lib.moe_forward_experts(ctypes.byref(cfg), d, d, ctypes.byref(weights), e0, e1,
+                                       s0, s1, d, d, ws_bytes, None)
+    assert call(2, 2, 0, 0) == B.MOE_ERR_INVALID_ARG        # empty expert range
+    assert call(0, 17, 0, 0) == B.MOE_ERR_INVALID_ARG       # past E
+    assert call(0, 4, 3, 2) == B.MOE_ERR_INVALID_ARG        # reversed shared range
+    assert call(0, 4, 0, 65) == B.MOE_ERR_INVALID_ARG       # past T
+    assert call(0, 4, 0, 8, ws_bytes=255) == B.MOE_ERR_WORKSPACE
+    no_shared = B.MoeWeights(None, None, d, d, None, None, None, None, None, None)
+    assert call(0, 4, 0, 8, weights=no_shared) == B.MOE_ERR_INVALID_ARG

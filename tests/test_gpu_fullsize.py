@@ -1,9 +1,11 @@
 """Parity at the full workload sizes, in the launch configuration bench.py times.
 
 Every token's routing (ids bit-exact, weights within 1e-5) and the whole
-dispatch grouping (bit-exact) are compared with the oracle; layer outputs are
-compared on a seeded sample of tokens (first and last token always included),
-which the oracle computes one by one.
+dispatch grouping (bit-exact) are compared with the oracle.  Layer outputs are
+compared on every token of the T=1024 workloads (prefill, W4A16 with group and
+channel scales) and of the decode batch; on the T=8192 workloads, on a seeded
+sample of tokens (first and last always included) plus, for the skewed one,
+every token of the last (ragged) 256-row tile of the three hottest experts.
 """
 import numpy as np
 import pytest
@@ -18,8 +20,18 @@ from helpers import WEIGHT_ABS, blob_parts, oracle_layer_rows, oracle_route, tol
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-SAMPLE = {"decode": 64, "prefill": 24, "skewed": 24, "w4a16": 24, "w4a16_decode": 64,
-          "dense_e64": 16, "w4a16_channel": 24}
+# tokens whose layer output is compared (None: all of them)
+SAMPLE = {"decode": None, "prefill": None, "skewed": 24, "w4a16": None, "w4a16_decode": None,
+          "dense_e64": 32, "w4a16_channel": None}
+
+
+def hot_tail_tokens(counts, offsets, perm, k, hottest=3, tile=256):
+    """Tokens of the last token tile of each of the ``hottest`` largest experts."""
+    rows = []
+    for e in np.argsort(-counts, kind="stable")[:hottest]:
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        rows.extend(range(lo + (hi - lo - 1) // tile * tile, hi))
+    return np.unique(perm[np.asarray(rows)] // k)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,8 +66,15 @@ def test_full_size(name):
         assert 0.15 <= empty <= 0.25, empty  # the workload's "~20% of experts get no token"
 
     n = SAMPLE[name]
-    rng = np.random.default_rng(2024)
-    rows = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, size=min(n, cfg.T),
-                                                                   replace=False)]))[:max(n, 2)]
+    if n is None:
+        rows = np.arange(cfg.T)
+    else:
+        rng = np.random.default_rng(2024)
+        rows = np.unique(np.concatenate([[0, cfg.T - 1],
+                                         rng.choice(cfg.T, size=min(n, cfg.T), replace=False)]))
+        if name == "skewed":
+            tail = hot_tail_tokens(c_ref, o_ref, p_ref, cfg.k)
+            assert tail.size > 0
+            rows = np.union1d(rows, tail)
     ref = oracle_layer_rows(inp, rows, ids_ref, w_ref)
-    tol_check(y_host(y)[rows], ref, what=f"{name} y[sample]")
+    tol_check(y_host(y)[rows], ref, what=f"{name} y[{rows.size} tokens]")

@@ -380,3 +380,55 @@ def test_bounded_wait_times_out_and_context_survives():
     assert 0.15 <= dt < 5.0, dt
     assert B.get_status(ws) == B.MOE_OK  # read-and-clear
     test_forward_parity("tiny")
+
+
+def test_status_is_sticky_until_read():
+    """An error recorded on a workspace survives later successful calls that use
+    the same workspace, and is cleared only by reading it (moe_get_status)."""
+    cfg = CONFIGS["tiny"]
+    host, dev = gpu_inputs(cfg)
+    ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
+    assert B.selftest_wait_timeout(ws, limit_ms=50, read_status=False) is None
+    y = B.forward(cfg, dev.x, dev, ws=ws)          # a later call on the same workspace
+    B.route(cfg, dev.x, dev.w_router, ws=ws)       # and a route call
+    torch.cuda.synchronize()
+    assert B.get_status(ws) == B.MOE_ERR_TIMEOUT   # still reported
+    assert B.get_status(ws) == B.MOE_OK            # cleared by the read
+    ids_ref, w_ref = oracle_route(host)
+    tol_check(y_host(y), oracle_layer_rows(host, np.arange(cfg.T), ids_ref, w_ref))
+
+
+@pytest.mark.parametrize("layout", ["sequential", "offset8"])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_repack_int4_sequential_to_pair_order(layout, in_place):
+    """Sequential-order words (value j in bits 4j..4j+3), packed here from that
+    definition, come out in the order the oracle reads: its exact dequantisation
+    with unit scales returns the original values.  1517 words: a ragged tail."""
+    rng = np.random.default_rng(11)
+    R, C = 37, 8 * 41
+    q = rng.integers(-8, 8, size=(R, C))
+    nib = ((q + 8) if layout == "offset8" else q) & 15
+    words = np.zeros((R, C // 8), np.uint64)
+    for j in range(8):
+        words |= nib[:, j::8].astype(np.uint64) << np.uint64(4 * j)
+    src = torch.from_numpy(words.astype(np.uint32).view(np.int32)).cuda()
+    code = B.MOE_INT4_SEQUENTIAL_OFFSET8 if layout == "offset8" else B.MOE_INT4_SEQUENTIAL
+    dst = B.repack_int4(src, dst=src if in_place else None, layout=code)
+    torch.cuda.synchronize()
+    unit = np.full(R, 0x3F80, np.uint16)  # bf16 1.0, one scale per row
+    got = oracle.dequant_w4(dst.cpu().numpy(), unit, 0)
+    assert np.array_equal(got, q.astype(np.float64))
+
+
+@pytest.mark.parametrize("sx,sw", [(-70, -70), (-64, -64), (-70, 0), (0, -130)])
+def test_route_bit_exact_at_tiny_magnitudes(sx, sw):
+    """Token and router rows scaled by 2^sx and 2^sw, so that the products
+    x_d * w_d (about 2^(sx+sw)) fall below the fp32 normal range (2^-126) where
+    fp32 products and the tensor core's partial sums are no longer exact or may
+    be flushed.  The decision must still be the fp64 definition's, bit for bit."""
+    cfg = MoEConfig("tiny_mag", T=64, D=256, E=16, I=64, Is=64, k=2)
+    host = make_inputs(cfg, device="cpu")
+    host.x = (host.x.float() * 2.0 ** sx).to(torch.bfloat16)
+    host.w_router = (host.w_router.float() * 2.0 ** sw).to(torch.bfloat16)
+    dev = host.to("cuda")
+    check_route(cfg, host, dev)

@@ -70,3 +70,91 @@ def test_static_permute_refuses_problems_beyond_its_scratch():
     rc = B.lib().moe_permute_static(ctypes.byref(B.config(cfg)), d, d, d, d, d, None, None, None)
     assert rc == B.MOE_ERR_SCRATCH_LIMIT
     assert "scratch" in B.strerror(rc)
+
+
+# Runs in a fresh process: the device memory comes from the driver API (no
+# torch), first in the device's primary context, then in a second context
+# created on the same device, then in the primary context again.  The fixed
+# array has another address in each context; every call must use the one of
+# the context current at the call.
+_CONTEXTS_SCRIPT = r"""
+import ctypes, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from sparse_moe_layer_router_gb300 import binding as B
+
+cu = ctypes.CDLL("libcuda.so.1")
+def ck(rc, what):
+    if rc != 0:
+        raise RuntimeError(f"{what} failed: {rc}")
+V = ctypes.c_void_p
+ck(cu.cuInit(0), "cuInit")
+dev = ctypes.c_int()
+ck(cu.cuDeviceGet(ctypes.byref(dev), 0), "cuDeviceGet")
+L = B.lib()
+T, E, k, D = 2000, 40, 3, 128   # 6000 pairs: the chunked path that uses the fixed array
+cfg = B.MoeConfig(T, D, E, 64, 64, k, 0, 128)
+rng = np.random.default_rng(5)
+ids = np.sort(np.argsort(rng.random((T, E)), axis=1)[:, :k], axis=1).astype(np.int32)
+blob = np.empty((T, 2, k), np.int32)
+blob[:, 0, :] = ids
+blob[:, 1, :] = np.full((T, k), 1.0 / k, np.float32).view(np.int32)
+
+def dalloc(nbytes):
+    p = ctypes.c_uint64()
+    ck(cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(nbytes)), "cuMemAlloc")
+    return p.value
+
+def run():
+    P = T * k
+    d_blob = dalloc(blob.nbytes)
+    ck(cu.cuMemcpyHtoD_v2(ctypes.c_uint64(d_blob), blob.ctypes.data_as(V), ctypes.c_size_t(blob.nbytes)), "HtoD")
+    sizes = [E, E + 1, P, P]
+    outs = [[dalloc(4 * n) for n in sizes] for _ in range(2)]
+    ws_n = L.moe_workspace_size(ctypes.byref(cfg), B.MOE_ENTRY_PERMUTE)
+    ws = dalloc(ws_n)
+    ck(cu.cuMemsetD8_v2(ctypes.c_uint64(ws), 0, ctypes.c_size_t(256)), "memset")
+    a, b = outs
+    ck(L.moe_permute(ctypes.byref(cfg), V(d_blob), V(a[0]), V(a[1]), V(a[2]), V(a[3]), None, None,
+                     V(ws), ws_n, None), "moe_permute")
+    ck(L.moe_permute_static(ctypes.byref(cfg), V(d_blob), V(b[0]), V(b[1]), V(b[2]), V(b[3]),
+                            None, None, None), "moe_permute_static")
+    ck(cu.cuCtxSynchronize(), "sync")
+    res = []
+    for bufs in outs:
+        host = []
+        for p, n in zip(bufs, sizes):
+            h = np.empty(n, np.int32)
+            ck(cu.cuMemcpyDtoH_v2(h.ctypes.data_as(V), ctypes.c_uint64(p), ctypes.c_size_t(4 * n)), "DtoH")
+            host.append(h)
+        res.append(host)
+    for p in [d_blob, ws] + outs[0] + outs[1]:
+        ck(cu.cuMemFree_v2(ctypes.c_uint64(p)), "cuMemFree")
+    for x, y in zip(*res):
+        assert np.array_equal(x, y)
+    return res[1]
+
+primary = V()
+ck(cu.cuDevicePrimaryCtxRetain(ctypes.byref(primary), dev), "retain")
+ck(cu.cuCtxSetCurrent(primary), "set primary")
+r1 = run()
+other = V()
+ck(cu.cuCtxCreate_v2(ctypes.byref(other), 0, dev), "cuCtxCreate")   # now current
+r2 = run()
+ck(cu.cuCtxDestroy_v2(other), "cuCtxDestroy")
+ck(cu.cuCtxSetCurrent(primary), "set primary again")
+r3 = run()
+for x, y, z in zip(r1, r2, r3):
+    assert np.array_equal(x, y) and np.array_equal(x, z)
+print("contexts ok")
+"""
+
+
+def test_static_permute_in_a_second_context_on_the_same_device():
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "-c", _CONTEXTS_SCRIPT, root], capture_output=True,
+                         text=True, timeout=300)
+    assert res.returncode == 0 and "contexts ok" in res.stdout, res.stdout + res.stderr
