@@ -72,6 +72,7 @@ struct TileInfo {
   int bn;
   int b_row;
   int k_blocks;
+  int n_tiles;  // token tiles of the group: each weight tile is read this many times
 };
 
 // Shared-memory parts common to both kernels.
@@ -162,6 +163,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmCommon<BN_MAX>& s, con
   const int rows = t.shared ? p.T_shared : s.off[t.e + 1] - s.off[t.e];
   const int row0 = t.shared ? 0 : s.off[t.e];
   const int n_tiles = (rows + BN_MAX - 1) / BN_MAX;
+  t.n_tiles = n_tiles;
   t.m = l / n_tiles;
   const int n = l - t.m * n_tiles;
   t.n_valid = min(BN_MAX, rows - n * BN_MAX);
@@ -459,7 +461,10 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      const uint64_t pol_w = policy_evict_first();
+      // Weight tiles read by one token tile stream through L2 (evict first);
+      // those of groups with several token tiles are read again by the
+      // neighbouring tiles of the walk and are kept (evict last).
+      const uint64_t pol_once = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -474,6 +479,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
                                           t.shared ? &tm_b8_s : &tm_b8};
         const uint32_t bytes = kAStage + static_cast<uint32_t>(t.bn) * 128u;
         const int row = tile_a_row(p, t);
+        const uint64_t pol_w = t.n_tiles > 1 ? pol_x : pol_once;
         for (int kb = 0; kb < t.k_blocks; ++kb) {
           if (!mbar_wait<true>(&s.empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
