@@ -43,6 +43,12 @@ constexpr int kBK = 64;
 constexpr int kAStage = kBM * kBK * 2;  // 16 KB bf16 operand tile
 constexpr int kMaxGroups = 1025;
 constexpr int kBaseThreads = 192;       // producer, MMA, 4 epilogue warps
+// The bf16 kernel runs 8 epilogue warps (two per TMEM lane quarter, each
+// taking every other 16-column chunk): its epilogue writes a tile's outputs
+// while the next tile's MMAs run, and with 256 token columns and fp32 outputs
+// four warps could not keep up.
+constexpr int kBf16EpiWarps = 8;
+constexpr int kBf16Threads = 64 + 32 * kBf16EpiWarps;
 
 // W4A16: packed stages of 128 rows x 128 B (256 int4 values = 4 k-blocks).
 // Shared-memory variant: two dequant groups of four warps (one tile row per
@@ -85,7 +91,7 @@ struct GemmCommon {
   int abort_flag;
   int tile_start[kMaxGroups + 1];
   int off[kMaxGroups];
-  float row_weight[4][BN_MAX];  // down epilogue: routing weight of each token row, per warp
+  float row_weight[8][BN_MAX];  // down epilogue: routing weight of each token row, per warp
 };
 
 template <int BN_MAX, int STAGES>
@@ -257,22 +263,27 @@ __device__ int build_tile_table(GemmCommon<BN_MAX>& s, const GemmParams& p, int 
 }
 
 template <int BN_MAX>
-__device__ __forceinline__ void init_common_barriers(GemmCommon<BN_MAX>& c) {
+__device__ __forceinline__ void init_common_barriers(GemmCommon<BN_MAX>& c, int epi_warps = 4) {
   for (int i = 0; i < 2; ++i) {
     mbar_init(&c.tfull[i], 1);
-    mbar_init(&c.tempty[i], 4);
+    mbar_init(&c.tempty[i], epi_warps);
   }
   mbar_init(&c.drain, 1);
   c.abort_flag = 0;
 }
 
-// Epilogue role (warps 2-5): TMEM accumulators -> h (SwiGLU, bf16) or o
+// Epilogue role (warps 2 .. 1+NE): TMEM accumulators -> h (SwiGLU, bf16) or o
 // (routing-weighted, fp32).  With NP = 2 the accumulator is the sum of two
-// partial accumulators 2 * BN_MAX columns apart (two MMA issuers).
-template <int BN_MAX, int NP = 1, bool kSleep = false>
+// partial accumulators 2 * BN_MAX columns apart (two MMA issuers).  With
+// NE = 8 two warps share each TMEM lane quarter and take alternate 16-column
+// chunks.
+template <int BN_MAX, int NP = 1, bool kSleep = false, int NE = 4>
 __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G, int ntiles,
                               uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
+  static_assert(NE == 4 || NE == 8, "one or two warps per TMEM lane quarter");
   const int sp = warp & 3;  // TMEM lanes 32*sp .. 32*sp+31
+  const int c_first = 16 * ((warp - 2) / 4);  // first 16-column chunk of this warp
+  constexpr int c_step = 16 * (NE / 4);
   float* wts = s.row_weight[warp - 2];
   int acc = 0;
   uint32_t acc_phase = 0;
@@ -309,7 +320,7 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
       const uint16_t* sc = t.shared ? p.wscale_s : p.wscale;
       row_scale = bf16_bits_to_float(__ldg(sc + tile_weight_row(p, t, 32 * sp + lane)));
     }
-    for (int c0 = 0; c0 < t.bn; c0 += 16) {
+    for (int c0 = c_first; c0 < t.bn; c0 += c_step) {
       uint32_t r[16];
       tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), r);
       if (NP == 2) {
@@ -403,7 +414,7 @@ __device__ __forceinline__ void load_token_tile(uint8_t* dst, const CUtensorMap*
 // bf16 weights
 // ==========================================================================
 template <int BN_MAX, int STAGES>
-__global__ void __launch_bounds__(kBaseThreads, 1)
+__global__ void __launch_bounds__(kBf16Threads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_a_s,
                         const __grid_constant__ CUtensorMap tm_b,
@@ -430,7 +441,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
-    init_common_barriers<BN_MAX>(cm);
+    init_common_barriers<BN_MAX>(cm, kBf16EpiWarps);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -447,7 +458,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
       prefetch_tmap(&tm_b8_s);
     }
   }
-  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kBaseThreads);
+  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kBf16Threads);
   if (warp == 1) {
     tmem_alloc(&cm.tmem_base, kTmemCols);
     tmem_relinquish();
@@ -550,7 +561,8 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
       mbar_wait_time_only(&cm.drain, 0);
     }
   } else {
-    epilogue_role<BN_MAX, 1, true>(cm, p, G, ntiles, tmem_base, abort_flag, warp, lane);
+    epilogue_role<BN_MAX, 1, true, kBf16EpiWarps>(cm, p, G, ntiles, tmem_base, abort_flag, warp,
+                                                  lane);
   }
 
   // The successor may launch once every CTA is past its tiles (a persistent
@@ -1281,7 +1293,7 @@ static cudaError_t launch_bf16(const GemmParams& p, const GemmMaps& m, int num_s
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return pdl_launch(kern, dim3(num_sms), dim3(kBaseThreads), smem, st, m.a, m.a_s, m.b, m.b_s,
+  return pdl_launch(kern, dim3(num_sms), dim3(kBf16Threads), smem, st, m.a, m.a_s, m.b, m.b_s,
                     m.b2, m.b2_s, m.b4, m.b4_s, m.b8, m.b8_s, p);
 }
 
