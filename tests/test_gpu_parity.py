@@ -22,6 +22,8 @@ pytestmark = pytest.mark.gpu
 
 SMALL = {
     "tiny": CONFIGS["tiny"],
+    # the largest k the entry points accept (32 experts per token)
+    "k32": MoEConfig("k32", T=40, D=256, E=48, I=64, Is=64, k=32),
     # several tiles in every direction with a ragged tail
     "ragged": MoEConfig("ragged", T=37, D=256, E=24, I=192, Is=128, k=3),
     # k = E: every token uses every expert
@@ -153,10 +155,12 @@ def test_router_logits_tensor_core_error_bound():
     print(f"worst |z - exact| / sum|x w| = {worst:.3e} (certification assumes 3.1e-05)")
 
 
-@pytest.mark.parametrize("T,E,k", [(100, 1000, 8), (2100, 1024, 8), (2100, 33, 3)])
+@pytest.mark.parametrize("T,E,k", [(100, 1000, 8), (2100, 1024, 8), (2100, 33, 3), (70, 64, 32),
+                                   (600, 1024, 32)])
 def test_route_bit_exact_wide_and_long(T, E, k):
-    """Many experts (up to 1024: 32 logits per lane in the select kernels) and batches
-    of 512 tokens or more (the warp-per-token select), with a ragged expert count."""
+    """Many experts (up to 1024: 32 logits per lane in the select kernels), batches
+    of 512 tokens or more (the warp-per-token select), a ragged expert count, and
+    the largest k the entry points accept (32)."""
     cfg = MoEConfig(f"r{T}x{E}", T=T, D=256, E=E, I=64, Is=64, k=k)
     host, dev = gpu_inputs(cfg)
     check_route(cfg, host, dev)
