@@ -206,6 +206,12 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 // the low bits of the two halves; XOR with 8 makes them offset binary (q + 8)
 // and 0x4300 | u is the bf16 of 128 + u (exact); subtracting 136 (exact) and
 // multiplying by the scale (one rounding) gives the pair, already in order.
+// The 0x4300 | u step is the classic magic-number integer-to-float
+// conversion (an integer placed in the mantissa of a float whose exponent is
+// fixed, the float of the offset then subtracted), the method low-bit
+// weight-only kernels use to dequantise, e.g. Kim et al., "Who Says Elephants
+// Can't Run: Bringing Large Scale MoE Models into Cloud Scale Production"
+// (2022).
 // kScale = false (channel-wise scales, applied in the epilogue): the exact q.
 template <bool kScale = true>
 __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
