@@ -953,7 +953,10 @@ struct W4TSmem {
   GemmCommon<64> c;
 };
 
-template <int PSTAGES, int TSTAGES, int ND>
+// SM: where the restore takes its scale from.  0: the group scales in global
+// memory; 1: the group scales from the tile's shared-memory table (TMA);
+// 2: channel-wise scales (the restore keeps q exact and the epilogue scales).
+template <int PSTAGES, int TSTAGES, int ND, int SM>
 __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
     grouped_gemm_w4t_kernel(const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_a_s,
@@ -978,7 +981,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.E + p.has_shared;
-  const bool table = p.scale_table != 0;
+  constexpr bool table = SM == 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < PSTAGES; ++i) {
@@ -1248,7 +1251,9 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
         for (int h = 0; h < kMyBlocks; ++h) {
           const int j = kSub * h + hd;
           const int g = ((kb0 + j) * kBK) / kGroup;
-          const uint16_t sbits = p.channel ? uint16_t{0x3F80} : table ? s.stab[sb][r * ngrp + g] : __ldg(srow + g);
+          const uint16_t sbits = SM == 2   ? uint16_t{0x3F80}
+                                 : SM == 1 ? s.stab[sb][r * ngrp + g]
+                                           : __ldg(srow + g);
           __nv_bfloat162 s2;
           s2.x = __ushort_as_bfloat16(sbits);
           s2.y = s2.x;
@@ -1257,7 +1262,7 @@ __global__ void __launch_bounds__(w4t_threads<ND>(), 1)
           uint32_t v[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 d = restore_word(words[c], s2, p.channel != 0);
+            const uint4 d = restore_word(words[c], s2, SM == 2);
             v[4 * c] = d.x;
             v[4 * c + 1] = d.y;
             v[4 * c + 2] = d.z;
@@ -1319,7 +1324,9 @@ template <int PSTAGES, int TSTAGES, int ND>
 static cudaError_t launch_w4t(const GemmParams& p, const GemmMaps& m, int num_sms,
                               cudaStream_t st) {
   const size_t smem = sizeof(W4TSmem<PSTAGES, TSTAGES>) + 1024;
-  auto kern = grouped_gemm_w4t_kernel<PSTAGES, TSTAGES, ND>;
+  auto kern = p.channel       ? grouped_gemm_w4t_kernel<PSTAGES, TSTAGES, ND, 2>
+              : p.scale_table ? grouped_gemm_w4t_kernel<PSTAGES, TSTAGES, ND, 1>
+                              : grouped_gemm_w4t_kernel<PSTAGES, TSTAGES, ND, 0>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1333,7 +1340,7 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int b
     if (bn_max == 64) return launch_bf16<64, 8>(p, maps, num_sms, st);
     if (bn_max == 256) return launch_bf16<256, 4>(p, maps, num_sms, st);
   } else if (quant == 1) {
-    if (bn_max == 64) return launch_w4t<6, 3, 16>(p, maps, num_sms, st);
+    if (bn_max == 64) return launch_w4t<6, 3, 8>(p, maps, num_sms, st);
     if (bn_max == 256) return launch_w4<256, 3, 2>(p, maps, num_sms, st);
   }
   return cudaErrorInvalidValue;
