@@ -80,3 +80,31 @@ def ep_forward(x_local: torch.Tensor, E: int, route_fn, experts_fn, group=None):
     n = x_local.shape[0]
     y_partial = experts_fn(x_all, blob_all, e0, e1, rank * n, (rank + 1) * n)
     return reduce_scatter_rows(y_partial, group), blob_all   # collective 3: outputs home
+
+
+def library_fns(cfg_local, cfg_all, w_router, bias, local_weights, shared_weights=None):
+    """(route_fn, experts_fn) for ep_forward backed by this library's kernels.
+
+    cfg_local     shapes of one rank's call to the router (T = tokens per rank).
+    cfg_all       shapes of the expert slice (T = all ranks' tokens, E = all experts).
+    w_router      bf16 [E, D] router weight (every rank holds it); bias fp32 [E] or None.
+    local_weights dict with this rank's experts: w_gate_up, w_down (and, for W4A16,
+                  s_gate_up, s_down), leading dimension e_end - e_begin.
+    shared_weights dict with ws_gate_up, ws_down (ss_gate_up, ss_down for W4A16).
+    """
+    from . import binding as B
+
+    sw = shared_weights or {}
+    weights = B.MoeWeights(None, None, B._p(local_weights["w_gate_up"]),
+                           B._p(local_weights["w_down"]), B._p(local_weights.get("s_gate_up")),
+                           B._p(local_weights.get("s_down")), B._p(sw.get("ws_gate_up")),
+                           B._p(sw.get("ws_down")), B._p(sw.get("ss_gate_up")),
+                           B._p(sw.get("ss_down")))
+
+    def route_fn(x_local):
+        return B.route(cfg_local, x_local, w_router, bias)
+
+    def experts_fn(x_all, blob_all, e0, e1, s0, s1):
+        return B.forward_experts(cfg_all, x_all, blob_all, weights, e0, e1, s0, s1)
+
+    return route_fn, experts_fn

@@ -102,3 +102,38 @@ def test_bad_ranges_rejected():
         with pytest.raises(B.MoeError) as ex:
             B.forward_experts(cfg, d, d, w, e0, e1, s0, s1, y_partial=d, ws=ws)
         assert ex.value.code == B.MOE_ERR_INVALID_ARG
+
+
+def test_ep_forward_one_rank_through_the_library():
+    """The expert-parallel step (route, the two all-gathers, the expert slice,
+    the reduce-scatter) with this library's kernels on a one-rank NCCL group:
+    the collectives are identities, so the result must match moe_forward's
+    layer output within the layer tolerance."""
+    import socket
+    import torch.distributed as dist
+    from sparse_moe_layer_router_gb300 import expert_parallel as ep
+
+    cfg = CASES["ep_bf16"]
+    host = make_inputs(cfg, device="cpu")
+    dev = host.to("cuda")
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    store = dist.TCPStore("127.0.0.1", port, 1, True)
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1)
+    try:
+        route_fn, experts_fn = ep.library_fns(
+            cfg, cfg, dev.w_router, dev.bias,
+            {"w_gate_up": dev.w_gate_up, "w_down": dev.w_down},
+            {"ws_gate_up": dev.ws_gate_up, "ws_down": dev.ws_down})
+        y_local, blob_all = ep.ep_forward(dev.x, cfg.E, route_fn, experts_fn)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    y_ref = B.forward(cfg, dev.x, dev)
+    ids_ref, w_ref = oracle_route(host)
+    ids, _ = blob_parts(blob_all)
+    assert np.array_equal(ids, ids_ref)
+    ref = oracle_layer_rows(host, np.arange(cfg.T), ids_ref, w_ref)
+    tol_check(y_local.double().cpu().numpy(), ref, what="expert-parallel step, one rank")
+    tol_check(y_ref.double().cpu().numpy(), y_local.double().cpu().numpy(), what="vs moe_forward")
