@@ -104,6 +104,7 @@ def test_bad_ranges_rejected():
         assert ex.value.code == B.MOE_ERR_INVALID_ARG
 
 
+@pytest.mark.timeout(300)
 def test_ep_forward_one_rank_through_the_library():
     """The expert-parallel step (route, the two all-gathers, the expert slice,
     the reduce-scatter) with this library's kernels on a one-rank NCCL group:
