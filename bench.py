@@ -336,7 +336,7 @@ def measure(cfg, inp, args, world, rank, dev, clocks_on, hbm_peak, bf16_peak, pe
     stream = torch.cuda.current_stream()
     ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD, dev)
     y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=dev)
-    W = B.weights_struct(inp)
+    W = B.weights_struct(inp, cfg)
 
     def step():
         B.forward(cfg, inp.x, W, y=y, ws=ws)

@@ -131,6 +131,45 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _need(t, name, dtype, numel):
+    """Reject a tensor of the wrong type, or one the kernels would read or write
+    past the end of (``numel`` elements at least).  Raw integer pointers pass
+    unchecked: their extent is the caller's responsibility."""
+    if not isinstance(t, torch.Tensor):
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: needs {numel} elements, has {t.numel()}")
+
+
+def _weight_spec(cfg, gate_up, shared, n_experts=None):
+    """(dtype, weight elements, scale elements) of one projection in the
+    format of moe_weights: bf16 rows, or int32 words of 8 int4 values plus bf16
+    scales (per group of ``group`` inputs, or one per row when group == 0)."""
+    i = cfg.Is if shared else cfg.I
+    rows, K = (2 * i, cfg.D) if gate_up else (cfg.D, i)
+    n = 1 if shared else (cfg.E if n_experts is None else n_experts)
+    if cfg.quant == MOE_QUANT_W4A16:
+        per_row = K // cfg.group if cfg.group > 0 else 1
+        return torch.int32, n * rows * K // 8, n * rows * per_row
+    return torch.bfloat16, n * rows * K, 0
+
+
+def _need_weights(cfg, inp, n_experts=None):
+    """Check the tensors of a MoEInputs-like object against cfg."""
+    bf = torch.bfloat16
+    _need(getattr(inp, "w_router", None), "w_router", bf, cfg.E * cfg.D)
+    _need(getattr(inp, "bias", None), "router_bias", torch.float32, cfg.E)
+    for gate_up, shared, w, s in ((True, False, "w_gate_up", "s_gate_up"),
+                                  (False, False, "w_down", "s_down"),
+                                  (True, True, "ws_gate_up", "ss_gate_up"),
+                                  (False, True, "ws_down", "ss_down")):
+        dt, nw, ns = _weight_spec(cfg, gate_up, shared, n_experts)
+        _need(getattr(inp, w, None), w, dt, nw)
+        _need(getattr(inp, s, None), s, bf, ns)
+
+
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -158,6 +197,10 @@ def route(cfg, x, w_router, bias=None, blob=None, ws=None, stream=None):
     """int32 blob [T, 2, k] (ids ascending, then fp32 weight bits)."""
     if blob is None:
         blob = torch.empty((cfg.T, 2, cfg.k), dtype=torch.int32, device=x.device)
+    _need(x, "x", torch.bfloat16, cfg.T * cfg.D)
+    _need(w_router, "w_router", torch.bfloat16, cfg.E * cfg.D)
+    _need(bias, "bias", torch.float32, cfg.E)
+    _need(blob, "blob", torch.int32, cfg.T * 2 * cfg.k)
     if ws is None:
         ws = workspace(cfg, MOE_ENTRY_ROUTE, x.device)
     _check(lib().moe_route(ctypes.byref(config(cfg)), _p(x), _p(w_router), _p(bias), _p(blob),
@@ -169,6 +212,9 @@ def router_logits(cfg, x, w_router, z=None, ws=None, stream=None):
     """fp32 [T, E] level-1 router logits x . Wr^T (tensor cores, no bias)."""
     if z is None:
         z = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=x.device)
+    _need(x, "x", torch.bfloat16, cfg.T * cfg.D)
+    _need(w_router, "w_router", torch.bfloat16, cfg.E * cfg.D)
+    _need(z, "z", torch.float32, cfg.T * cfg.E)
     if ws is None:
         ws = workspace(cfg, MOE_ENTRY_ROUTE, x.device)
     _check(lib().moe_router_logits(ctypes.byref(config(cfg)), _p(x), _p(w_router), _p(z), _p(ws),
@@ -187,12 +233,24 @@ def permute(cfg, blob, ws=None, stream=None, x=None, x_perm=None, out=None):
                torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev),
                torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev))
     counts, offsets, perm, inv = out
+    _need_permute(cfg, blob, counts, offsets, perm, inv, x, x_perm)
     if ws is None:
         ws = workspace(cfg, MOE_ENTRY_PERMUTE, dev)
     _check(lib().moe_permute(ctypes.byref(config(cfg)), _p(blob), _p(counts), _p(offsets), _p(perm),
                              _p(inv), _p(x), _p(x_perm), _p(ws), ws.numel(), _stream(stream)),
            "moe_permute")
     return counts, offsets, perm, inv
+
+
+def _need_permute(cfg, blob, counts, offsets, perm, inv, x, x_perm):
+    P = cfg.T * cfg.k
+    _need(blob, "blob", torch.int32, cfg.T * 2 * cfg.k)
+    _need(counts, "counts", torch.int32, cfg.E)
+    _need(offsets, "offsets", torch.int32, cfg.E + 1)
+    _need(perm, "perm_pair", torch.int32, P)
+    _need(inv, "inv_row", torch.int32, P)
+    _need(x, "x", torch.bfloat16, cfg.T * cfg.D)
+    _need(x_perm, "x_perm", torch.bfloat16, P * cfg.D)
 
 
 def permute_static(cfg, blob, stream=None, x=None, x_perm=None):
@@ -202,6 +260,7 @@ def permute_static(cfg, blob, stream=None, x=None, x_perm=None):
     offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
     perm = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
     inv = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
+    _need_permute(cfg, blob, counts, offsets, perm, inv, x, x_perm)
     _check(lib().moe_permute_static(ctypes.byref(config(cfg)), _p(blob), _p(counts), _p(offsets),
                                     _p(perm), _p(inv), _p(x), _p(x_perm), _stream(stream)),
            "moe_permute_static")
@@ -212,6 +271,24 @@ def grouped_gemm(cfg, op, a, offsets, w, out, *, a_row_index=None, w_scales=None
                  blob=None, a_shared=None, w_shared=None, ws_scales=None, out_shared=None,
                  ws=None, stream=None):
     """One grouped GEMM launch (see moe_gemm_args in include/moe.h)."""
+    P, bf, f32 = cfg.T * cfg.k, torch.bfloat16, torch.float32
+    gate_up = op == MOE_OP_GATE_UP_SWIGLU
+    K, K_s = (cfg.D, cfg.D) if gate_up else (cfg.I, cfg.Is)
+    _need(a, "a", bf, (cfg.T if a_row_index is not None else P) * K)
+    _need(a_row_index, "a_row_index", torch.int32, P)
+    _need(offsets, "offsets", torch.int32, cfg.E + 1)
+    dt, nw, ns = _weight_spec(cfg, gate_up, False)
+    _need(w, "w", dt, nw)
+    _need(w_scales, "w_scales", bf, ns)
+    _need(out, "out", bf if gate_up else f32, P * (cfg.I if gate_up else cfg.D))
+    _need(perm_pair, "perm_pair", torch.int32, P)
+    _need(blob, "blob", torch.int32, cfg.T * 2 * cfg.k)
+    _need(a_shared, "a_shared", bf, cfg.T * K_s)
+    dt, nw, ns = _weight_spec(cfg, gate_up, True)
+    _need(w_shared, "w_shared", dt, nw)
+    _need(ws_scales, "ws_scales", bf, ns)
+    _need(out_shared, "out_shared", bf if gate_up else f32,
+          cfg.T * (cfg.Is if gate_up else cfg.D))
     args = MoeGemmArgs(op, _p(a), _p(a_row_index), _p(offsets), _p(w), _p(w_scales),
                        _p(perm_pair), _p(blob), _p(out), _p(a_shared), _p(w_shared),
                        _p(ws_scales), _p(out_shared))
@@ -225,13 +302,21 @@ def grouped_gemm(cfg, op, a, offsets, w, out, *, a_row_index=None, w_scales=None
 def combine(cfg, o, o_shared, inv_row, y=None, stream=None):
     if y is None:
         y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=o.device)
+    P = cfg.T * cfg.k
+    _need(o, "o", torch.float32, P * cfg.D)
+    _need(o_shared, "o_shared", torch.float32, cfg.T * cfg.D)
+    _need(inv_row, "inv_row", torch.int32, P)
+    _need(y, "y", torch.bfloat16, cfg.T * cfg.D)
     _check(lib().moe_combine(ctypes.byref(config(cfg)), _p(o), _p(o_shared), _p(inv_row), _p(y),
                              _stream(stream)), "moe_combine")
     return y
 
 
-def weights_struct(inp) -> MoeWeights:
-    """MoeWeights from a MoEInputs (all tensors on the GPU)."""
+def weights_struct(inp, cfg=None) -> MoeWeights:
+    """MoeWeights from a MoEInputs (all tensors on the GPU); with ``cfg`` the
+    tensors are first checked against the shapes the layer reads."""
+    if cfg is not None:
+        _need_weights(cfg, inp)
     return MoeWeights(_p(inp.w_router), _p(inp.bias), _p(inp.w_gate_up), _p(inp.w_down),
                       _p(inp.s_gate_up), _p(inp.s_down), _p(inp.ws_gate_up), _p(inp.ws_down),
                       _p(inp.ss_gate_up), _p(inp.ss_down))
@@ -240,9 +325,11 @@ def weights_struct(inp) -> MoeWeights:
 def forward(cfg, x, weights, y=None, ws=None, stream=None):
     """Whole layer; ``weights`` is a MoeWeights or a MoEInputs on the GPU."""
     if not isinstance(weights, MoeWeights):
-        weights = weights_struct(weights)
+        weights = weights_struct(weights, cfg)
     if y is None:
         y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=x.device)
+    _need(x, "x", torch.bfloat16, cfg.T * cfg.D)
+    _need(y, "y", torch.bfloat16, cfg.T * cfg.D)
     if ws is None:
         ws = workspace(cfg, MOE_ENTRY_FORWARD, x.device)
     _check(lib().moe_forward(ctypes.byref(config(cfg)), _p(x), ctypes.byref(weights), _p(y), _p(ws),
@@ -253,10 +340,12 @@ def forward(cfg, x, weights, y=None, ws=None, stream=None):
 def forward_host(cfg, x_host, weights, y_host, ws, stream=None):
     """Whole layer with host x / y (pinned CPU tensors); caller synchronises."""
     if not isinstance(weights, MoeWeights):
-        weights = weights_struct(weights)
+        weights = weights_struct(weights, cfg)
     for t in (x_host, y_host):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("forward_host takes contiguous CPU tensors")
+    _need(x_host, "x_host", torch.bfloat16, cfg.T * cfg.D)
+    _need(y_host, "y_host", torch.bfloat16, cfg.T * cfg.D)
     _check(lib().moe_forward_host(ctypes.byref(config(cfg)), ctypes.c_void_p(x_host.data_ptr()),
                                   ctypes.byref(weights), ctypes.c_void_p(y_host.data_ptr()),
                                   _p(ws), ws.numel(), _stream(stream)), "moe_forward_host")
@@ -268,9 +357,13 @@ def forward_experts(cfg, x, blob, weights, e_begin, e_end, shared_begin=0, share
     """fp32 [T, D] partial output of the routed experts [e_begin, e_end) (``weights``
     holds those experts only) plus the shared expert on tokens [shared_begin, shared_end)."""
     if not isinstance(weights, MoeWeights):
+        _need_weights(cfg, weights, n_experts=max(int(e_end) - int(e_begin), 0))
         weights = weights_struct(weights)
     if y_partial is None:
         y_partial = torch.empty((cfg.T, cfg.D), dtype=torch.float32, device=x.device)
+    _need(x, "x", torch.bfloat16, cfg.T * cfg.D)
+    _need(blob, "blob", torch.int32, cfg.T * 2 * cfg.k)
+    _need(y_partial, "y_partial", torch.float32, cfg.T * cfg.D)
     if ws is None:
         ws = workspace(cfg, MOE_ENTRY_FORWARD_EXPERTS, x.device)
     _check(lib().moe_forward_experts(ctypes.byref(config(cfg)), _p(x), _p(blob),
@@ -286,6 +379,7 @@ def repack_int4(src, dst=None, layout=MOE_INT4_SEQUENTIAL, stream=None):
         raise ValueError("packed int4 words are int32")
     if dst is None:
         dst = torch.empty_like(src)
+    _need(dst, "dst", torch.int32, src.numel())
     _check(lib().moe_repack_int4(_p(src), _p(dst), src.numel(), int(layout), _stream(stream)),
            "moe_repack_int4")
     return dst

@@ -2,6 +2,7 @@
 every function include/moe.h declares, sizes workspaces, and rejects invalid
 arguments on the host (before any CUDA call)."""
 import ctypes
+import dataclasses
 import os
 import re
 
@@ -145,3 +146,42 @@ def test_repack_and_expert_slice_host_validation(lib):
     assert call(0, 4, 0, 8, ws_bytes=255) == B.MOE_ERR_WORKSPACE
     no_shared = B.MoeWeights(None, None, d, d, None, None, None, None, None, None)
     assert call(0, 4, 0, 8, weights=no_shared) == B.MOE_ERR_INVALID_ARG
+
+
+def test_binding_rejects_tensors_the_kernels_would_overrun(lib):
+    """The binding checks dtype and extent of every tensor against cfg before
+    the call: an fp32 output given as bf16 (half the bytes), a short buffer or
+    int4 words given as bf16 raise ValueError on the host."""
+    import torch
+    cfg = CONFIGS["tiny"]
+    P = cfg.T * cfg.k
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    h = torch.empty((P, cfg.I), dtype=bf)
+    off = torch.empty(cfg.E + 1, dtype=i32)
+    wd = torch.empty((cfg.E, cfg.D, cfg.I), dtype=bf)
+    perm = torch.empty(P, dtype=i32)
+    blob = torch.empty((cfg.T, 2, cfg.k), dtype=i32)
+    o_half = torch.empty((P, cfg.D), dtype=bf)       # down output is fp32
+    with pytest.raises(ValueError, match="out: expected torch.float32"):
+        B.grouped_gemm(cfg, B.MOE_OP_DOWN_WEIGHTED, h, off, wd, o_half, perm_pair=perm, blob=blob)
+    o_short = torch.empty((P - 1, cfg.D), dtype=f32)
+    with pytest.raises(ValueError, match="out: needs"):
+        B.grouped_gemm(cfg, B.MOE_OP_DOWN_WEIGHTED, h, off, wd, o_short, perm_pair=perm, blob=blob)
+    with pytest.raises(ValueError, match="o: expected torch.float32"):
+        B.combine(cfg, o_half, None, perm, y=torch.empty((cfg.T, cfg.D), dtype=bf))
+    with pytest.raises(ValueError, match="y_partial: needs"):
+        B.forward_experts(cfg, torch.empty((cfg.T, cfg.D), dtype=bf), blob,
+                          B.MoeWeights(), 0, 1, y_partial=torch.empty(cfg.T, dtype=f32))
+    with pytest.raises(ValueError, match="blob: needs"):
+        B.permute(cfg, torch.empty(cfg.T, dtype=i32))
+    with pytest.raises(ValueError, match="dst: needs"):
+        B.repack_int4(torch.empty(64, dtype=i32), torch.empty(63, dtype=i32))
+    # W4A16: packed int32 words, bf16 scales per group of inputs
+    w4 = dataclasses.replace(cfg, quant=B.MOE_QUANT_W4A16, group=128)
+    with pytest.raises(ValueError, match="w: expected torch.int32"):
+        B.grouped_gemm(w4, B.MOE_OP_DOWN_WEIGHTED, h, off, wd, torch.empty((P, cfg.D), dtype=f32),
+                       perm_pair=perm, blob=blob)
+    # right dtypes and extents get as far as the device check
+    with pytest.raises(ValueError, match="CUDA"):
+        B.grouped_gemm(cfg, B.MOE_OP_DOWN_WEIGHTED, h, off, wd, torch.empty((P, cfg.D), dtype=f32),
+                       perm_pair=perm, blob=blob)

@@ -97,10 +97,11 @@ def test_bad_ranges_rejected():
     d = torch.zeros(16, dtype=torch.int32, device="cuda")
     w = B.MoeWeights(None, None, B._p(d), B._p(d), None, None, B._p(d), B._p(d), None, None)
     ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD_EXPERTS)
+    p = d.data_ptr()  # raw pointers: the library's own range checks, not the binding's
     for e0, e1, s0, s1 in [(3, 3, 0, 0), (-1, 2, 0, 0), (0, cfg.E + 1, 0, 0), (0, 2, 5, 4),
                            (0, 2, 0, cfg.T + 1)]:
         with pytest.raises(B.MoeError) as ex:
-            B.forward_experts(cfg, d, d, w, e0, e1, s0, s1, y_partial=d, ws=ws)
+            B.forward_experts(cfg, p, p, w, e0, e1, s0, s1, y_partial=p, ws=ws)
         assert ex.value.code == B.MOE_ERR_INVALID_ARG
 
 
