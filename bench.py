@@ -1,5 +1,5 @@
 """Benchmark of the MoE layer forward: decode step (T=64, D=4096, E=512, I=1024,
-top-10) as the headline, and the T=1024 prefill chunk beside it.
+top-10) as the headline, and every other synthetic workload beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -15,9 +15,14 @@ expert included) over one batch of synthetic input, through the C ABI.
   roofline  the dominant kernel (grouped gate/up GEMM): algorithmic bytes per
             launch / its mean CUDA-event duration inside a timed pass of the
             path split into its ABI calls, against the measured HBM copy peak.
-  cpu_baseline  the fp64 oracle on this host's cores over the same batch.
-  configs.prefill  the same measurements for the T=1024 prefill chunk on the
-            same expert weights (the metric's second configuration).
+  cpu_baseline  the fp64 oracle on this host's cores over the same batch (at
+            most its first 1024 tokens).
+  configs   the same measurements for the other workloads: the T=1024 prefill
+            chunk (the metric's second configuration) and the skewed T=8192
+            batch on the same expert weights, the tiny layer, W4A16 at T=1024
+            (group and channel-wise scales) and T=64, and the compute-bound
+            T=8192 batch on 64 experts.  A workload whose kernels record a
+            device error carries "error" instead of numbers.
 
 After warm-up, after the timed steps, after the split pass and after the e2e
 steps the workspace status words are read: a kernel that recorded a device
@@ -52,6 +57,11 @@ NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e nominal (context for the measured-copy 
 GEMM_SOURCES = [os.path.join(ROOT, "sparse_moe_layer_router_gb300", "csrc", f)
                 for f in ("grouped_gemm.cu", "common.cuh")]
 L2_BYTES = 129 * 2**20
+# Measured beside the decode headline, in this order (the first two reuse the
+# decode expert weights; the W4A16 decode batch reuses the W4A16 weights).
+EXTRA_WORKLOADS = ("prefill", "skewed", "tiny", "w4a16", "w4a16_decode", "w4a16_channel",
+                   "dense_e64")
+ORACLE_SAMPLE_TOKENS = 1024
 
 
 def parse():
@@ -65,7 +75,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
-                    help="with the default decode workload, skip the T=1024 prefill line")
+                    help="with the default decode workload, skip the other workloads")
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads measured beside the decode headline")
     return ap.parse_args()
 
 
@@ -227,13 +239,14 @@ def oracle_pass(cfg, rows, host_x, host_wr, host_bias, experts, shared):
                           quant=cfg.quant, group=cfg.group)
 
 
-def oracle_host_inputs(inp):
-    """Host copies of the inputs and of every expert the batch touches."""
+def oracle_host_inputs(inp, n_tokens=None):
+    """Host copies of the inputs (the first ``n_tokens`` token rows, default all)
+    and of every expert those rows touch."""
     import numpy as np
     import oracle
     from sparse_moe_layer_router_gb300.synthetic import as_u16
     cfg = inp.cfg
-    x = as_u16(inp.x)
+    x = as_u16(inp.x if n_tokens is None else inp.x[:n_tokens])
     wr = as_u16(inp.w_router)
     bias = None if inp.bias is None else inp.bias.cpu().numpy()
     ids, _ = oracle.route(x, wr, cfg.k, bias)
@@ -254,17 +267,18 @@ def oracle_host_inputs(inp):
 
 
 def cpu_baseline(cfg, inputs, min_seconds=10.0, max_passes=20):
-    """Full-batch oracle passes until ``min_seconds`` of CPU work: (tokens/s, cores, passes)."""
+    """Oracle passes over the sampled token rows (all rows of ``inputs``) until
+    ``min_seconds`` of CPU work: (tokens/s, cores, passes, rows per pass)."""
     import numpy as np
     import oracle
-    rows = np.arange(cfg.T)
+    rows = np.arange(inputs[0].shape[0])
     done, t0 = 0, time.perf_counter()
     while True:
         oracle_pass(cfg, rows, *inputs)
         done += 1
         dt = time.perf_counter() - t0
         if dt >= min_seconds or done >= max_passes:
-            return cfg.T * done / dt, oracle.num_threads(), done
+            return len(rows) * done / dt, oracle.num_threads(), done, len(rows)
 
 
 def run_reference(args, cfg, base_config, local):
@@ -477,16 +491,50 @@ def measure(cfg, inp, args, world, rank, dev, clocks_on, hbm_peak, bf16_peak, pe
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        inputs = oracle_host_inputs(inp)
-        val, cores, passes = cpu_baseline(cfg, inputs)
+        inputs = oracle_host_inputs(inp, min(cfg.T, ORACLE_SAMPLE_TOKENS))
+        val, cores, passes, n = cpu_baseline(cfg, inputs)
+        what = (f"the full {cfg.name} batch ({cfg.T} tokens" if n == cfg.T
+                else f"the first {n} of the {cfg.name} batch's {cfg.T} tokens (")
         cpu = {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"the full {cfg.name} batch ({cfg.T} tokens; fp64 routing + layer) "
+               "sample": f"{what}{'; ' if n == cfg.T else ''}fp64 routing + layer) "
                          f"x{passes} passes"}
         del inputs
     del ws, y
     return {"value": value, "ms_per_step": ms_step, "roofline": roofline, "layer": layer,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps, "workload": workload_desc(cfg)}
+
+
+def measure_extra(names, inp, args, world, rank, dev, hbm_peak, bf16_peak, peak_src):
+    """The workloads beside the headline, one after the other.  Inputs that share
+    expert weights with the previous ones (same D, E, I, Is, k, quant, group) reuse
+    them with fresh token rows and router bias; others are drawn anew."""
+    import torch
+    from sparse_moe_layer_router_gb300.synthetic import CONFIGS, make_inputs, with_tokens
+    same = ("D", "E", "I", "Is", "k", "quant", "group", "seed")
+    out = {}
+    cur = inp
+    for name in names:
+        cfg = CONFIGS[name]
+        if all(getattr(cfg, f) == getattr(cur.cfg, f) for f in same):
+            w = with_tokens(cur, cfg)
+        else:
+            cur = w = None
+            torch.cuda.empty_cache()
+            cur = w = make_inputs(cfg, device=dev)
+        try:
+            r = measure(cfg, w, args, world, rank, dev, not args.no_clocks, hbm_peak, bf16_peak,
+                        peak_src, with_traffic=False)
+        except DeviceError as e:
+            out[name] = {"config": {"workload": workload_desc(cfg)}, "error": str(e)}
+            continue
+        lay = r["layer"]["algorithmic_bytes"]
+        l2 = ("no flush: the touched expert weights streamed each step exceed L2 (129 MB)"
+              if lay > L2_BYTES else
+              f"no flush: the whole layer's {lay / 2**20:.1f} MiB fit in L2 (launch-bound)")
+        out[name] = {"metric": METRIC, "unit": "tokens/s", "steps": args.steps,
+                     "config": {"workload": r.pop("workload"), "T": cfg.T, "l2": l2}, **r}
+    return out
 
 
 # ------------------------------------------------------------------ main
@@ -529,13 +577,8 @@ def main():
                    peak_src, with_traffic=args.config == "decode")
     extra = {}
     if args.config == "decode" and not args.decode_only:
-        # the metric's second configuration: the T=1024 prefill chunk on the same
-        # expert weights (only the token rows differ)
-        pre = with_tokens(inp, CONFIGS["prefill"])
-        r = measure(pre.cfg, pre, args, world, rank, dev, not args.no_clocks, hbm_peak,
-                    bf16_peak, peak_src, with_traffic=False)
-        extra["prefill"] = {"metric": METRIC, "unit": "tokens/s", "steps": args.steps,
-                            "config": {"workload": r.pop("workload"), "T": pre.cfg.T}, **r}
+        names = [n for n in args.extra.split(",") if n]
+        extra = measure_extra(names, inp, args, world, rank, dev, hbm_peak, bf16_peak, peak_src)
 
     if rank == 0:
         line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,

@@ -181,12 +181,15 @@ def tokens(cfg: MoEConfig, device="cpu") -> torch.Tensor:
 
 def with_tokens(inp: MoEInputs, cfg: MoEConfig) -> MoEInputs:
     """Inputs of ``cfg``, a configuration that differs from ``inp.cfg`` only in
-    the token count T: the same router and expert weights (the expert weights
-    depend on (seed, E, D, I, Is, quant, group) only), fresh token rows."""
-    same = ("D", "E", "I", "Is", "k", "quant", "group", "zipf_s", "zipf_alpha", "seed")
+    the token count T and the router bias: the same router and expert weights
+    (the expert weights depend on (seed, E, D, I, Is, quant, group) only), fresh
+    token rows and the bias of ``cfg`` (as make_inputs draws them)."""
+    same = ("D", "E", "I", "Is", "k", "quant", "group", "seed")
     if any(getattr(cfg, f) != getattr(inp.cfg, f) for f in same):
-        raise ValueError(f"{cfg.name} differs from {inp.cfg.name} in more than T")
-    return replace(inp, cfg=cfg, x=tokens(cfg, inp.x.device))
+        raise ValueError(f"{cfg.name} differs from {inp.cfg.name} in more than T and the bias")
+    dev = inp.x.device
+    bias = zipf_bias(cfg.E, cfg.zipf_s, cfg.zipf_alpha, cfg.seed).to(dev) if cfg.zipf_s > 0 else None
+    return replace(inp, cfg=cfg, x=tokens(cfg, dev), bias=bias)
 
 
 def make_inputs(cfg: MoEConfig, device="cpu", weight_device=None) -> MoEInputs:

@@ -49,3 +49,23 @@ def test_single_rank_is_identity():
     import bench
     assert bench.slowest_rank(3.5, 1, "cpu") == 3.5
     assert bench.job_tokens_per_s(1, 64, 100, 2.0) == 3200.0
+
+
+def test_extra_workloads_exist_and_share_weights_where_bench_reuses_them():
+    """Every workload the default run measures is a known configuration, and
+    with_tokens (used to reuse expert weights between neighbouring workloads)
+    gives exactly the inputs make_inputs draws for the new configuration."""
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    from sparse_moe_layer_router_gb300.synthetic import CONFIGS, make_inputs, with_tokens
+    for n in bench.EXTRA_WORKLOADS:
+        assert n in CONFIGS, n
+    base = CONFIGS["tiny"]
+    other = base.with_(name="tiny_skewed", T=96, zipf_s=1.2, zipf_alpha=0.9)
+    a = with_tokens(make_inputs(base), other)
+    b = make_inputs(other)
+    for f in ("x", "w_router", "bias", "w_gate_up", "w_down", "ws_gate_up", "ws_down"):
+        assert torch.equal(getattr(a, f), getattr(b, f)), f
+    with pytest.raises(ValueError):
+        with_tokens(make_inputs(base), base.with_(name="tiny_e8", E=8))
