@@ -54,6 +54,11 @@
  *      weight = q * s, exact in fp64.
  *  R8  Everything after routing is computed in fp64 with no intermediate
  *      rounding.
+ *  R21 NaN logits (a NaN in the token row or the router row): a NaN ranks
+ *      below every number, NaNs among themselves by index, so a token always
+ *      gets k distinct ids.  The weights depend only on the selected logits
+ *      (the renormalisation cancels the full denominator): a NaN among the
+ *      unselected logits does not reach them; a selected NaN makes them NaN.
  *
  * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (contraction is off
  * so that x86 and Arm hosts give the same bits).
@@ -154,8 +159,17 @@ int oracle_router_logits(int T, int D, int E, const uint16_t *x,
 }
 
 /* ------------------------------------------------------------------ */
-/* Top-k selection and weights for one token (readings R2, R3, R4).    */
+/* Top-k selection and weights for one token (readings R2, R3, R4,     */
+/* R21).                                                               */
 /* ------------------------------------------------------------------ */
+/* Does logit a rank above logit b?  Numbers by value; a NaN ranks below every
+   number and never above another NaN (reading R21).  Equal ranks keep the
+   lower index because experts are visited in ascending order. */
+static int ranks_above(double a, double b) {
+  if (isnan(a)) return 0;
+  return isnan(b) || a > b;
+}
+
 static void select_token(int E, int k, const double *z, int32_t *ids,
                          double *w, unsigned char *taken) {
   memset(taken, 0, (size_t)E);
@@ -164,7 +178,7 @@ static void select_token(int E, int k, const double *z, int32_t *ids,
     int best = -1;
     for (int e = 0; e < E; ++e) {
       if (taken[e]) continue;
-      if (best < 0 || z[e] > z[best]) best = e;
+      if (best < 0 || ranks_above(z[e], z[best])) best = e;
     }
     taken[best] = 1;
   }
@@ -172,12 +186,19 @@ static void select_token(int E, int k, const double *z, int32_t *ids,
   int n = 0;
   for (int e = 0; e < E; ++e)
     if (taken[e]) ids[n++] = e;
-  /* Softmax over all E experts ... */
-  double m = z[0];
-  for (int e = 1; e < E; ++e)
-    if (z[e] > m) m = z[e];
+  /* Softmax over all E experts ... (a NaN logit has no probability to give
+     the denominator; since the renormalisation below cancels the
+     denominator, only a NaN among the selected logits reaches the weights) */
+  double m = 0.0;
+  int have_m = 0;
+  for (int e = 0; e < E; ++e)
+    if (!isnan(z[e]) && (!have_m || z[e] > m)) {
+      m = z[e];
+      have_m = 1;
+    }
   double denom = 0.0;
-  for (int e = 0; e < E; ++e) denom += exp(z[e] - m);
+  for (int e = 0; e < E; ++e)
+    if (!isnan(z[e])) denom += exp(z[e] - m);
   /* ... then renormalise the selected probabilities to sum to one. */
   double sel = 0.0;
   for (int j = 0; j < k; ++j) {

@@ -170,6 +170,58 @@ def test_route_hand_worked_example():
     np.testing.assert_allclose(w, g["weights"], rtol=1e-15, atol=1e-16)
 
 
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def test_route_nan_logits_rank_below_every_number():
+    """Reading R21: experts whose router row holds a NaN (NaN logits) are never
+    chosen while k finite experts remain; the ids equal exhaustive search over
+    the finite experts alone, and the weights equal the renormalised softmax of
+    the selected exact logits (scipy), untouched by the unselected NaNs."""
+    T, D, E, k = 9, 8, 7, 3
+    x, wr = small_inputs(T, D, E, 21)
+    nan_rows = [1, 4]
+    wr_nan = wr.copy()
+    for e in nan_rows:
+        wr_nan[e, 3] = BF16_NAN
+    ids, w = oracle.route(x, wr_nan, k)
+    finite = [e for e in range(E) if e not in nan_rows]
+    z = exact_logits(x, wr[finite])
+    for t in range(T):
+        sel = [finite[i] for i in brute_topk(z[t], k)]
+        assert ids[t].tolist() == sel
+        zsel = np.array([float(z[t][finite.index(e)]) for e in sel])
+        np.testing.assert_allclose(w[t], scipy.special.softmax(zsel), rtol=1e-12, atol=0)
+
+
+def test_route_fewer_finite_logits_than_k_fill_with_lowest_nan_indices():
+    """Reading R21: with only two finite logits and k = 4, both finite experts
+    and the two lowest-index NaN experts are chosen; a selected NaN makes the
+    token's weights NaN."""
+    T, D, E, k = 3, 8, 5, 4
+    x, wr = small_inputs(T, D, E, 22)
+    for e in (0, 2, 3):
+        wr[e, 0] = BF16_NAN
+    ids, w = oracle.route(x, wr, k)
+    assert (ids == np.array([0, 1, 2, 4], np.int32)).all()
+    assert np.isnan(w).all()
+
+
+def test_route_nan_token_row_takes_lowest_indices_and_spares_other_tokens():
+    """A token row with a NaN has NaN logits everywhere: ids 0..k-1 (reading
+    R21), NaN weights; the other tokens route exactly as without it."""
+    T, D, E, k = 6, 8, 9, 3
+    x, wr = small_inputs(T, D, E, 23)
+    ids0, w0 = oracle.route(x, wr, k)
+    xn = x.copy()
+    xn[2, 5] = BF16_NAN
+    ids, w = oracle.route(xn, wr, k)
+    assert ids[2].tolist() == list(range(k)) and np.isnan(w[2]).all()
+    keep = [t for t in range(T) if t != 2]
+    assert (ids[keep] == ids0[keep]).all()
+    assert np.array_equal(w[keep], w0[keep])
+
+
 def test_router_logits_index_order_sum():
     """Exact products summed left to right in fp64: check against exact rationals
     rounded after every addition (the definition's rounding sequence)."""
