@@ -39,6 +39,17 @@
  *   - Return 0 on success or a negative MOE_ERR_* code.  Argument and shape
  *     errors are detected on the host and launch nothing.  Device-side wait
  *     timeouts are reported through moe_get_status().
+ *   - Index data read from caller buffers (expert ids in a blob, offsets,
+ *     perm_pair, a_row_index, inv_row) is checked on the device: a value
+ *     outside its range is clamped into it, so every access stays inside the
+ *     buffers whatever they hold (the affected tokens' outputs are then
+ *     meaningless), and the entries that take a workspace record
+ *     MOE_ERR_INVALID_ARG in its status word (moe_get_status).  The data
+ *     written by moe_route and moe_permute is always in range.
+ *   - NaN logits (from NaN in x, the router weights or the bias) rank below
+ *     every number, NaNs among themselves by index: every token gets k
+ *     distinct ids; a token whose selected logits include a NaN gets NaN
+ *     weights, and a NaN in a token row reaches only that token's output.
  *   - There is no fallback path: unsupported shapes return MOE_ERR_UNSUPPORTED.
  *   - Kernels are built for sm_103a only; other devices get MOE_ERR_UNSUPPORTED.
  */
@@ -54,7 +65,8 @@ extern "C" {
 
 /* ---- error codes ---- */
 #define MOE_OK 0
-#define MOE_ERR_INVALID_ARG (-1)  /* null pointer, k < 1, k > E, T < 1, ...       */
+#define MOE_ERR_INVALID_ARG (-1)  /* null pointer, k < 1, k > E, T < 1, ...; on the
+                                     device: an index out of range (moe_get_status) */
 #define MOE_ERR_UNSUPPORTED (-2)  /* shape/format outside the kernels' envelope     */
 #define MOE_ERR_WORKSPACE (-3)    /* workspace null or smaller than required        */
 #define MOE_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed           */

@@ -26,8 +26,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   float4 acc = o_shared ? __ldg(o_shared + static_cast<size_t>(t) * D4 + c)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
   const int32_t* rows = inv_row + static_cast<size_t>(t) * k;
+  const int P = T * k;
   for (int j = 0; j < k; ++j) {
-    const float4 v = __ldg(o + static_cast<size_t>(__ldg(rows + j)) * D4 + c);
+    // a row outside [0, T*k) (an inv_row that moe_permute did not write) is
+    // clamped, so the load stays inside o
+    const int r = min(max(__ldg(rows + j), 0), P - 1);
+    const float4 v = __ldg(o + static_cast<size_t>(r) * D4 + c);
     acc.x += v.x;
     acc.y += v.y;
     acc.z += v.z;

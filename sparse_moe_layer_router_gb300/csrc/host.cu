@@ -250,6 +250,8 @@ Layout layout(const moe_config* c, int entry) {
       break;
     case MOE_ENTRY_GROUPED_GEMM:
       L.xperm = cv.take(P * D * 2);  // gathered activation rows when a_row_index is given
+      L.offsets = cv.take((E + 1) * 4);  // the caller's offsets, clamped and monotone
+      L.perm = cv.take(P * 4);           // the caller's perm_pair, clamped
       break;
     case MOE_ENTRY_FORWARD_EXPERTS:
       L.chunk = cv.take(chunks * E * 4);
@@ -362,8 +364,8 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   if (a->a_row_index) {
     if (!gate_up) return MOE_ERR_INVALID_ARG;
     void* xp = xperm_override ? xperm_override : at<void>(ws, L.xperm);
-    const int grc =
-        cuda_rc(launch_gather_rows(a->a, a->a_row_index, P, c->D, 1, xp, nullptr, nullptr, st));
+    const int grc = cuda_rc(launch_gather_rows(a->a, a->a_row_index, P, c->D, 1, c->T, xp,
+                                               nullptr, nullptr, at<int>(ws, 0), st));
     if (grc) return grc;
     b_routed = xp;
   }
@@ -505,11 +507,11 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   if (rc) return rc;
   rc = cuda_rc(launch_permute(at<int32_t>(ws, L.blob), c->T, c->k, c->E, at<int32_t>(ws, L.chunk),
                               at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
-                              at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), st));
+                              at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), at<int>(ws, 0), st));
   if (rc) return rc;
   // dispatch: token rows in grouped order (pair index / k = token)
-  rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k,
-                                  at<void>(ws, L.xperm), nullptr, nullptr, st));
+  rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k, c->T,
+                                  at<void>(ws, L.xperm), nullptr, nullptr, nullptr, st));
   if (rc) return rc;
   moe_gemm_args g{};
   g.op = MOE_OP_GATE_UP_SWIGLU;
@@ -552,13 +554,13 @@ int forward_experts_impl(const moe_config* c, const DevInfo& dev, const void* x,
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int rc = cuda_rc(launch_permute(blob, c->T, c->k, c->E, at<int32_t>(ws, L.chunk),
                                   at<int32_t>(ws, L.counts), offsets, at<int32_t>(ws, L.perm),
-                                  at<int32_t>(ws, L.inv), st));
+                                  at<int32_t>(ws, L.inv), at<int>(ws, 0), st));
   if (rc) return rc;
   // grouped rows of the local experts: [offsets[e0], offsets[e1])
   const int32_t* row_lo = offsets + e0;
   const int32_t* row_hi = offsets + e1;
-  rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k,
-                                  at<void>(ws, L.xperm), row_lo, row_hi, st));
+  rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k, c->T,
+                                  at<void>(ws, L.xperm), row_lo, row_hi, nullptr, st));
   if (rc) return rc;
   const int ts = s1 - s0;
   const void* x_sh = static_cast<const char*>(x) + static_cast<size_t>(s0) * c->D * 2;
@@ -668,10 +670,10 @@ int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   rc = cuda_rc(launch_permute(blob, cfg->T, cfg->k, cfg->E, at<int32_t>(ws, L.chunk), counts,
-                              offsets, perm_pair, inv_row, st));
+                              offsets, perm_pair, inv_row, at<int>(ws, 0), st));
   if (rc || !x) return rc;
-  return cuda_rc(
-      launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, x_perm, nullptr, nullptr, st));
+  return cuda_rc(launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, cfg->T, x_perm,
+                                    nullptr, nullptr, nullptr, st));
 }
 
 int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* counts,
@@ -705,8 +707,17 @@ int moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws,
   Layout L;
   rc = begin(cfg, MOE_ENTRY_GROUPED_GEMM, ws, ws_bytes, &dev, &L);
   if (rc) return rc;
-  return gemm_impl(cfg, dev, args, ws, L, static_cast<cudaStream_t>(stream), nullptr, cfg->E,
-                   cfg->T);
+  // The kernels trust offsets and perm_pair (the forward entries pass arrays
+  // moe_permute wrote); caller arrays are first copied into range.
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  moe_gemm_args g = *args;
+  g.offsets = at<int32_t>(ws, L.offsets);
+  g.perm_pair = args->perm_pair ? at<int32_t>(ws, L.perm) : nullptr;
+  rc = cuda_rc(launch_sanitize_gemm_indices(args->offsets, cfg->E + 1, cfg->T * cfg->k,
+                                            at<int32_t>(ws, L.offsets), args->perm_pair,
+                                            at<int32_t>(ws, L.perm), at<int>(ws, 0), st));
+  if (rc) return rc;
+  return gemm_impl(cfg, dev, &g, ws, L, st, nullptr, cfg->E, cfg->T);
 }
 
 int moe_combine(const moe_config* cfg, const float* o, const float* o_shared,

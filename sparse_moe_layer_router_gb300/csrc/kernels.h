@@ -52,14 +52,25 @@ cudaError_t launch_router_select(const float* z_part, int S, int T, int D, int E
                                  int32_t* blob, int* counters, cudaStream_t st);
 
 // ---- dispatch (permute.cu)
+// Expert ids outside [0, E) are clamped into it and, with a non-null status
+// word, recorded there as MOE_ERR_INVALID_ARG.
 cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,
                            int32_t* counts, int32_t* offsets, int32_t* perm_pair,
-                           int32_t* inv_row, cudaStream_t st);
+                           int32_t* inv_row, int* status, cudaStream_t st);
 // out[r] = a[idx[r] / div] for every row r, or (row_lo, row_hi non-NULL: device
-// pointers to two row indices) only for *row_lo <= r < *row_hi.
+// pointers to two row indices) only for *row_lo <= r < *row_hi.  Source rows
+// outside [0, src_rows) are clamped (and recorded as for launch_permute).
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
-                               void* out, const int32_t* row_lo, const int32_t* row_hi,
-                               cudaStream_t st);
+                               int src_rows, void* out, const int32_t* row_lo,
+                               const int32_t* row_hi, int* status, cudaStream_t st);
+// Caller index arrays made safe for the grouped GEMM: offsets_out[i] = the
+// running maximum of offsets[0..i] clamped into [0, rows] (monotone, so every
+// group's row range lies inside [0, rows)); perm_out[r] = perm_pair[r] clamped
+// into [0, rows) (perm_pair may be NULL).  A value that needed either is
+// recorded as MOE_ERR_INVALID_ARG in *status.
+cudaError_t launch_sanitize_gemm_indices(const int32_t* offsets, int n_offsets, int rows,
+                                         int32_t* offsets_out, const int32_t* perm_pair,
+                                         int32_t* perm_out, int* status, cudaStream_t st);
 // Capacity (int32 entries) of the fixed device array behind moe_permute_static.
 constexpr long kStaticPermuteScratchInts = 65536;
 cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int32_t* counts,

@@ -18,14 +18,26 @@
 
 namespace moe {
 
-__device__ __forceinline__ int pair_expert(const int32_t* __restrict__ blob, int k, int p) {
+// Expert id of pair p.  An id outside [0, E) (a blob that moe_route did not
+// write) sets `bad` and is clamped to the nearest valid expert, so that every
+// count, offset and position stays in bounds; the caller records the error.
+__device__ __forceinline__ int pair_expert(const int32_t* __restrict__ blob, int k, int E, int p,
+                                           bool& bad) {
   const int t = p / k, j = p - t * k;
-  return blob[static_cast<size_t>(t) * 2 * k + j];
+  const int e = blob[static_cast<size_t>(t) * 2 * k + j];
+  if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) return e;
+  bad = true;
+  return e < 0 ? 0 : E - 1;
+}
+
+__device__ __forceinline__ void report_invalid(bool bad, int* status) {
+  if (bad && status) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
 }
 
 __global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __restrict__ blob,
                                                             int P, int k, int E,
-                                                            int32_t* __restrict__ chunk_cnt) {
+                                                            int32_t* __restrict__ chunk_cnt,
+                                                            int* __restrict__ status) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int hist[];
@@ -33,7 +45,10 @@ __global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __res
   __syncthreads();
   const int p0 = blockIdx.x * kPermuteChunk;
   const int p1 = min(P, p0 + kPermuteChunk);
-  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) atomicAdd(&hist[pair_expert(blob, k, p)], 1);
+  bool bad = false;
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x)
+    atomicAdd(&hist[pair_expert(blob, k, E, p, bad)], 1);
+  report_invalid(bad, status);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     chunk_cnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
@@ -99,6 +114,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
 __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const int32_t* __restrict__ blob, int P, int k, int E, const int32_t* __restrict__ chunk_base,
     int32_t* __restrict__ perm_pair, int32_t* __restrict__ inv_row) {
+  bool bad = false;  // reported by the count kernel
   pdl_wait();
   pdl_trigger();
   extern __shared__ int wcnt[];  // [8][E]
@@ -108,7 +124,8 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
   constexpr int seg = kPermuteChunk / 8;
   const int p0 = blockIdx.x * kPermuteChunk + wid * seg;
   const int p1 = min(P, p0 + seg);
-  for (int p = p0 + lane; p < p1; p += 32) atomicAdd(&wcnt[wid * E + pair_expert(blob, k, p)], 1);
+  for (int p = p0 + lane; p < p1; p += 32)
+    atomicAdd(&wcnt[wid * E + pair_expert(blob, k, E, p, bad)], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = chunk_base[static_cast<size_t>(blockIdx.x) * E + e];
@@ -124,7 +141,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
   for (int pb = p0; pb < p1; pb += 32) {
     const int p = pb + lane;
     const bool valid = p < p1;
-    const int e = valid ? pair_expert(blob, k, p) : -1;
+    const int e = valid ? pair_expert(blob, k, E, p, bad) : -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     int pos = 0;
     if (valid) pos = my[e] + __popc(peers & lt_mask);
@@ -140,18 +157,25 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
 
 // out[r][:] = a[idx[r] / div][:]  (D bf16 per row, 16-byte vectors); with a
 // row range (device pointers row_lo, row_hi) only for *row_lo <= r < *row_hi.
+// A source row outside [0, src_rows) is clamped into it and recorded in
+// `status` (MOE_ERR_INVALID_ARG) when that is non-null.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ a,
                                                           const int32_t* __restrict__ idx,
                                                           int rows, int vec_per_row, int div,
-                                                          uint4* __restrict__ out,
+                                                          int src_rows, uint4* __restrict__ out,
                                                           const int32_t* __restrict__ row_lo,
-                                                          const int32_t* __restrict__ row_hi) {
+                                                          const int32_t* __restrict__ row_hi,
+                                                          int* __restrict__ status) {
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.x;
   if (r >= rows) return;
   if (row_lo && (r < __ldg(row_lo) || r >= __ldg(row_hi))) return;
-  const int src = idx[r] / div;
+  int src = idx[r] / div;
+  if (static_cast<unsigned>(src) >= static_cast<unsigned>(src_rows)) {
+    if (threadIdx.x == 0 && status) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+    src = src < 0 ? 0 : src_rows - 1;
+  }
   const uint4* s = a + static_cast<size_t>(src) * vec_per_row;
   uint4* d = out + static_cast<size_t>(r) * vec_per_row;
   for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = __ldg(s + i);
@@ -164,7 +188,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 constexpr int kPermuteOneBlockMaxPairs = 4096;
 __global__ void __launch_bounds__(1024) permute_one_block_kernel(
     const int32_t* __restrict__ blob, int P, int k, int E, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ perm_pair, int32_t* __restrict__ inv_row) {
+    int32_t* __restrict__ offsets, int32_t* __restrict__ perm_pair, int32_t* __restrict__ inv_row,
+    int* __restrict__ status) {
+  bool bad = false;
   pdl_wait();
   pdl_trigger();
   extern __shared__ int wc[];  // [32][E], then [32] warp sums
@@ -176,7 +202,8 @@ __global__ void __launch_bounds__(1024) permute_one_block_kernel(
   __syncthreads();
   const int seg = (P + 31) / 32;
   const int p0 = wid * seg, p1 = min(P, p0 + seg);
-  for (int p = p0 + lane; p < p1; p += 32) atomicAdd(&wc[wid * E + pair_expert(blob, k, p)], 1);
+  for (int p = p0 + lane; p < p1; p += 32) atomicAdd(&wc[wid * E + pair_expert(blob, k, E, p, bad)], 1);
+  report_invalid(bad, status);
   __syncthreads();
   for (int e0 = 0; e0 < E; e0 += 1024) {
     const int e = e0 + threadIdx.x;
@@ -222,7 +249,7 @@ __global__ void __launch_bounds__(1024) permute_one_block_kernel(
   for (int pb = p0; pb < p1; pb += 32) {
     const int p = pb + lane;
     const bool valid = p < p1;
-    const int e = valid ? pair_expert(blob, k, p) : -1;
+    const int e = valid ? pair_expert(blob, k, E, p, bad) : -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     int pos = 0;
     if (valid) pos = my[e] + __popc(peers & lt_mask);
@@ -236,9 +263,75 @@ __global__ void __launch_bounds__(1024) permute_one_block_kernel(
   }
 }
 
+// Offsets for the grouped GEMM from a caller: one warp; lane i takes a
+// contiguous chunk, clamps it into [0, rows] and keeps the running maximum
+// (a warp max-scan carries it across chunks), so the copy is monotone.
+__global__ void __launch_bounds__(32) sanitize_offsets_kernel(const int32_t* __restrict__ in,
+                                                              int n, int rows,
+                                                              int32_t* __restrict__ out,
+                                                              int* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x;
+  const int chunk = (n + 31) / 32;
+  const int i0 = lane * chunk, i1 = min(n, i0 + chunk);
+  bool bad = false;
+  int run = 0;
+  for (int i = i0; i < i1; ++i) {
+    const int v = in[i];
+    const int c = min(max(v, 0), rows);
+    bad |= c != v || c < run;
+    run = max(run, c);
+  }
+  int incl = run;  // max over chunks 0..lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int m = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl = max(incl, m);
+  }
+  int prev = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) prev = 0;
+  // a chunk that starts below the previous chunks' maximum is a decrease too
+  if (i0 < i1) bad |= min(max(in[i0], 0), rows) < prev;
+  run = prev;
+  for (int i = i0; i < i1; ++i) {
+    run = max(run, min(max(in[i], 0), rows));
+    out[i] = run;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0 && status)
+    atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+}
+
+// out[i] = in[i] clamped into [0, hi), recording any change.
+__global__ void __launch_bounds__(256) clamp_rows_kernel(const int32_t* __restrict__ in, int n,
+                                                         int hi, int32_t* __restrict__ out,
+                                                         int* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
+  bool bad = false;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int v = in[i];
+    const bool ok = static_cast<unsigned>(v) < static_cast<unsigned>(hi);
+    bad |= !ok;
+    out[i] = ok ? v : (v < 0 ? 0 : hi - 1);
+  }
+  report_invalid(bad, status);
+}
+
+cudaError_t launch_sanitize_gemm_indices(const int32_t* offsets, int n_offsets, int rows,
+                                         int32_t* offsets_out, const int32_t* perm_pair,
+                                         int32_t* perm_out, int* status, cudaStream_t st) {
+  cudaError_t e = pdl_launch(sanitize_offsets_kernel, dim3(1), dim3(32), 0, st, offsets,
+                             n_offsets, rows, offsets_out, status);
+  if (e != cudaSuccess || !perm_pair) return e;
+  const int blocks = min((rows + 255) / 256, 1024);
+  return pdl_launch(clamp_rows_kernel, dim3(blocks), dim3(256), 0, st, perm_pair, rows, rows,
+                    perm_out, status);
+}
+
 cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* chunk_cnt,
                            int32_t* counts, int32_t* offsets, int32_t* perm_pair,
-                           int32_t* inv_row, cudaStream_t st) {
+                           int32_t* inv_row, int* status, cudaStream_t st) {
   const int P = T * k;
   const size_t smem_one = (static_cast<size_t>(32) * E + 32) * sizeof(int);
   if (P <= kPermuteOneBlockMaxPairs && smem_one <= 200 * 1024) {
@@ -249,7 +342,7 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
       if (e != cudaSuccess) return e;
     }
     return pdl_launch(permute_one_block_kernel, dim3(1), dim3(1024), smem_one, st, blob, P, k, E,
-                      counts, offsets, perm_pair, inv_row);
+                      counts, offsets, perm_pair, inv_row, status);
   }
   const int B = (P + kPermuteChunk - 1) / kPermuteChunk;
   const size_t smem_count = static_cast<size_t>(E) * sizeof(int);
@@ -261,7 +354,7 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = pdl_launch(permute_count_kernel, dim3(B), dim3(256), smem_count, st, blob, P, k,
-                             E, chunk_cnt);
+                             E, chunk_cnt, status);
   if (e != cudaSuccess) return e;
   e = pdl_launch(permute_scan_kernel, dim3(1), dim3(1024), 0, st, chunk_cnt, B, E, counts, offsets);
   if (e != cudaSuccess) return e;
@@ -270,11 +363,11 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
 }
 
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
-                               void* out, const int32_t* row_lo, const int32_t* row_hi,
-                               cudaStream_t st) {
+                               int src_rows, void* out, const int32_t* row_lo,
+                               const int32_t* row_hi, int* status, cudaStream_t st) {
   return pdl_launch(gather_rows_kernel, dim3(rows), dim3(256), 0, st,
-                    static_cast<const uint4*>(a), idx, rows, D / 8, div, static_cast<uint4*>(out),
-                    row_lo, row_hi);
+                    static_cast<const uint4*>(a), idx, rows, D / 8, div, src_rows,
+                    static_cast<uint4*>(out), row_lo, row_hi, status);
 }
 
 // ------------------------------------------------------------------
@@ -371,9 +464,9 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
   int32_t* table = nullptr;
   cudaError_t e = static_scratch(&table);
   if (e != cudaSuccess) return e;
-  e = launch_permute(blob, T, k, E, table, counts, offsets, perm_pair, inv_row, st);
+  e = launch_permute(blob, T, k, E, table, counts, offsets, perm_pair, inv_row, nullptr, st);
   if (e != cudaSuccess || !x) return e;
-  return launch_gather_rows(x, perm_pair, T * k, D, k, x_perm, nullptr, nullptr, st);
+  return launch_gather_rows(x, perm_pair, T * k, D, k, T, x_perm, nullptr, nullptr, nullptr, st);
 }
 
 }  // namespace moe

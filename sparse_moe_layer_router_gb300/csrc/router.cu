@@ -349,12 +349,68 @@ __device__ double warp_exact_logit(const __nv_bfloat16* __restrict__ xr,
   return __shfl_sync(0xffffffffu, acc, 0);
 }
 
-// Order used for selection: larger value first, lower index on an exact tie.
+// Order used for selection: larger value first, lower index on an exact tie;
+// a NaN logit orders below every number (-inf included), NaNs among
+// themselves by index.  Every search starts from the sentinel (NaN, INT_MAX),
+// which any expert beats, so each of the k rounds picks an expert whatever
+// the logits hold and the blob always gets k distinct ids in [0, E).
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
+  const bool vn = v != v, bn = bv != bv;
+  if (vn || bn) return bn && (!vn || e < be);
   return v > bv || (v == bv && e < be);
 }
 __device__ __forceinline__ bool better_d(double v, int e, double bv, int be) {
+  const bool vn = v != v, bn = bv != bv;
+  if (vn || bn) return bn && (!vn || e < be);
   return v > bv || (v == bv && e < be);
+}
+__device__ __forceinline__ float sentinel_f() { return __int_as_float(0x7fc00000); }
+__device__ __forceinline__ double sentinel_d() {
+  return __longlong_as_double(0x7ff8000000000000ll);
+}
+// The same order for numbers only (no operand is NaN), from the sentinel
+// (-inf, INT_MAX).
+__device__ __forceinline__ bool better_num(float v, int e, float bv, int be) {
+  return v > bv || (v == bv && e < be);
+}
+
+// k rounds of warp arg-max: each takes the best expert not yet in `sel` and
+// lowers min_lo to its v - r.  kNan selects the NaN-aware order; without a
+// NaN logit the plain comparisons give the same order.
+template <bool kNan, int VPL>
+__device__ __forceinline__ void topk_rounds(const float (&v)[VPL], const float (&r)[VPL], int E,
+                                            int k, int lane, uint32_t& sel, float& min_lo) {
+  for (int j = 0; j < k; ++j) {
+    float bv = kNan ? sentinel_f() : -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((sel >> i) & 1u) &&
+          (kNan ? better(v[i], e, bv, be) : better_num(v[i], e, bv, be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (kNan ? better(ov, oe, bv, be) : better_num(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) {
+      const int i = be >> 5;
+#pragma unroll
+      for (int q = 0; q < VPL; ++q)
+        if (q == i) {
+          sel |= 1u << q;
+          min_lo = fminf(min_lo, v[q] - r[q]);
+        }
+    }
+  }
 }
 
 // One 256-thread block per token.  All threads sum the split-K partials
@@ -439,38 +495,16 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     }
   }
 
-  // k rounds of warp arg-max under (value desc, index asc).
+  // k rounds of warp arg-max under (value desc, index asc); the NaN-aware
+  // order only for a token with a NaN logit (one warp vote).
   float min_lo = INFINITY;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+  bool nan_here = false;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((sel >> i) & 1u) && better(v[i], e, bv, be)) {
-        bv = v[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) {
-      const int i = be >> 5;
-#pragma unroll
-      for (int q = 0; q < VPL; ++q)
-        if (q == i) {
-          sel |= 1u << q;
-          min_lo = fminf(min_lo, v[q] - r[q]);
-        }
-    }
-  }
+  for (int i = 0; i < VPL; ++i) nan_here |= v[i] != v[i];
+  if (__any_sync(0xffffffffu, nan_here))
+    topk_rounds<true>(v, r, E, k, lane, sel, min_lo);
+  else
+    topk_rounds<false>(v, r, E, k, lane, sel, min_lo);
   float max_hi = -INFINITY;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
@@ -559,7 +593,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
     }
     uint32_t chosen = 0;
     for (int j = 0; j < slots; ++j) {
-      float bv = -INFINITY;
+      float bv = sentinel_f();
       int be = 0x7fffffff;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
@@ -616,7 +650,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(
       __syncwarp();
       chosen = 0;
       for (int j = 0; j < slots; ++j) {
-        double bv = -INFINITY;
+        double bv = sentinel_d();
         int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
@@ -736,38 +770,16 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(
     }
   }
 
-  // k rounds of warp arg-max under (value desc, index asc).
+  // k rounds of warp arg-max under (value desc, index asc); the NaN-aware
+  // order only for a token with a NaN logit (one warp vote).
   float min_lo = INFINITY;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+  bool nan_here = false;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((sel >> i) & 1u) && better(v[i], e, bv, be)) {
-        bv = v[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) {
-      const int i = be >> 5;
-#pragma unroll
-      for (int q = 0; q < VPL; ++q)
-        if (q == i) {
-          sel |= 1u << q;
-          min_lo = fminf(min_lo, v[q] - r[q]);
-        }
-    }
-  }
+  for (int i = 0; i < VPL; ++i) nan_here |= v[i] != v[i];
+  if (__any_sync(0xffffffffu, nan_here))
+    topk_rounds<true>(v, r, E, k, lane, sel, min_lo);
+  else
+    topk_rounds<false>(v, r, E, k, lane, sel, min_lo);
   float max_hi = -INFINITY;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
@@ -837,7 +849,7 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(
     }
     uint32_t chosen = 0;
     for (int j = 0; j < slots; ++j) {
-      float bv = -INFINITY;
+      float bv = sentinel_f();
       int be = 0x7fffffff;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
@@ -894,7 +906,7 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(
       __syncwarp();
       chosen = 0;
       for (int j = 0; j < slots; ++j) {
-        double bv = -INFINITY;
+        double bv = sentinel_d();
         int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {

@@ -117,6 +117,76 @@ def test_route_near_ties_refined_exactly():
     assert refined > 0
 
 
+def _route_poisoned(cfg, dev):
+    """moe_route into a blob filled with -1 first: every entry must be written."""
+    blob = torch.full((cfg.T, 2, cfg.k), -1, dtype=torch.int32, device="cuda")
+    ws = B.workspace(cfg, B.MOE_ENTRY_ROUTE)
+    B.route(cfg, dev.x, dev.w_router, dev.bias, blob=blob, ws=ws)
+    torch.cuda.synchronize()
+    assert B.get_status(ws) == B.MOE_OK
+    return blob_parts(blob)
+
+
+@pytest.mark.parametrize("T", [80, 600])
+def test_route_nan_logits_rank_last(T):
+    """NaN router rows and NaN token rows (reading R21): a NaN logit ranks below
+    every number.  ids bit-exact with the oracle (k distinct ids in [0, E) for
+    every token, all written), weights NaN exactly where the oracle's are,
+    the others within the weight tolerance.  T = 600 runs the warp-per-token
+    select kernel."""
+    cfg = MoEConfig(f"nan{T}", T=T, D=256, E=40, I=64, Is=64, k=4)
+    host = make_inputs(cfg, device="cpu")
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    host.w_router[7, 11] = nan
+    host.w_router[30, 0] = nan
+    host.x[5, 3] = nan
+    host.x[T - 17, 200] = nan
+    dev = host.to("cuda")
+    ids, w = _route_poisoned(cfg, dev)
+    ids_ref, w_ref = oracle_route(host)
+    assert np.array_equal(ids, ids_ref)
+    assert ((ids >= 0) & (ids < cfg.E)).all() and (np.diff(ids, axis=1) > 0).all()
+    assert np.array_equal(np.isnan(w), np.isnan(w_ref))
+    np.testing.assert_allclose(w, w_ref, rtol=0, atol=WEIGHT_ABS)
+    assert ids[5].tolist() == [0, 1, 2, 3] and np.isnan(w[5]).all()
+    assert not np.isin(ids[[t for t in range(T) if t not in (5, T - 17)]], [7, 30]).any()
+
+
+def test_route_fewer_finite_logits_than_k():
+    """A NaN bias on all but three of twelve experts with k = 5: each token gets
+    the three finite experts and the two lowest-index NaN experts (reading R21),
+    NaN weights, as the oracle."""
+    cfg = MoEConfig("nan_bias", T=70, D=256, E=12, I=64, Is=64, k=5)
+    host = make_inputs(cfg, device="cpu")
+    bias = torch.full((cfg.E,), float("nan"), dtype=torch.float32)
+    bias[[2, 6, 11]] = torch.tensor([0.5, -0.25, 0.0])
+    host.bias = bias
+    dev = host.to("cuda")
+    ids, w = _route_poisoned(cfg, dev)
+    ids_ref, w_ref = oracle_route(host)
+    assert np.array_equal(ids, ids_ref)
+    assert (ids == np.array([0, 1, 2, 6, 11], np.int32)).all()
+    assert np.isnan(w).all() and np.isnan(w_ref).all()
+
+
+def test_forward_nan_token_row_stays_in_its_row():
+    """A NaN in one token row: that token's output row is NaN, every other row
+    matches the oracle (the NaN travels in its own GEMM column only)."""
+    cfg = SMALL["ragged"]
+    host = make_inputs(cfg, device="cpu")
+    host.x[3, 17] = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    dev = host.to("cuda")
+    ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
+    y = B.forward(cfg, dev.x, dev, ws=ws)
+    torch.cuda.synchronize()
+    assert B.get_status(ws) == B.MOE_OK
+    yh = y_host(y)
+    assert np.isnan(yh[3]).all()
+    ids, w = oracle_route(host)
+    rows = np.array([t for t in range(cfg.T) if t != 3])
+    tol_check(yh[rows], oracle_layer_rows(host, rows, ids, w), what="rows without the NaN")
+
+
 def _bf16(a):
     return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
 
