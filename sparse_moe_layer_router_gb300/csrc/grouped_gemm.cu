@@ -300,15 +300,47 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
       // accumulator is ready: row r holds pair p = perm_pair[r] (token p / k,
       // slot p % k); the shared group has weight 1.
       __syncwarp();
-      for (int j = lane; j < t.n_valid; j += 32) {
-        float wgt = 1.0f;
-        if (!t.shared) {
-          const int pr = __ldg(p.perm_pair + t.b_row + j);
-          const int tk = pr / p.k;
-          wgt = __int_as_float(
-              __ldg(p.blob + static_cast<size_t>(tk) * 2 * p.k + p.k + (pr - tk * p.k)));
+      if constexpr (NE == 8) {
+        // The bf16 kernel: every lane issues all its perm_pair loads, then all
+        // its blob loads, so a 256-row tile waits for two memory latencies
+        // rather than two per row (with one loop iteration per row this chain
+        // outlasted the tile's MMAs at T = 8192).  The W4A16 kernels keep the
+        // loop below: the unrolled form cost them 4-6%.
+        constexpr int kPer = BN_MAX / 32;
+        int prs[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int j = lane + 32 * u;
+          prs[u] = (!t.shared && j < t.n_valid) ? __ldg(p.perm_pair + t.b_row + j) : 0;
         }
-        wts[j] = wgt;
+        float wv[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int j = lane + 32 * u;
+          wv[u] = 1.0f;
+          if (!t.shared && j < t.n_valid) {
+            const int pr = prs[u];
+            const int tk = pr / p.k;
+            wv[u] = __int_as_float(
+                __ldg(p.blob + static_cast<size_t>(tk) * 2 * p.k + p.k + (pr - tk * p.k)));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int j = lane + 32 * u;
+          if (j < t.n_valid) wts[j] = wv[u];
+        }
+      } else {
+        for (int j = lane; j < t.n_valid; j += 32) {
+          float wgt = 1.0f;
+          if (!t.shared) {
+            const int pr = __ldg(p.perm_pair + t.b_row + j);
+            const int tk = pr / p.k;
+            wgt = __int_as_float(
+                __ldg(p.blob + static_cast<size_t>(tk) * 2 * p.k + p.k + (pr - tk * p.k)));
+          }
+          wts[j] = wgt;
+        }
       }
       __syncwarp();
     }
