@@ -60,7 +60,7 @@ L2_BYTES = 129 * 2**20
 # Measured beside the decode headline, in this order (the first two reuse the
 # decode expert weights; the W4A16 decode batch reuses the W4A16 weights).
 EXTRA_WORKLOADS = ("prefill", "skewed", "tiny", "w4a16", "w4a16_decode", "w4a16_channel",
-                   "dense_e64")
+                   "dense_e64", "w4a16_dense_e64")
 ORACLE_SAMPLE_TOKENS = 1024
 
 

@@ -78,6 +78,10 @@ CONFIGS = {
     # Compute-bound grouped GEMM: T=8192 on 64 experts, ~1280 rows per expert
     # (256-row token tiles), where the tensor pipe rather than HBM bounds the GEMMs.
     "dense_e64": MoEConfig("dense_e64", T=8192, D=4096, E=64, I=1024, Is=1024, k=10),
+    # W4A16 on the compute-bound shape (T=8192 on 64 experts, 256-row token
+    # tiles): the case of the W4A16 kernel that restores into shared memory.
+    "w4a16_dense_e64": MoEConfig("w4a16_dense_e64", T=8192, D=4096, E=64, I=1024, Is=1024,
+                                 k=10, quant=1, group=128),
     # Zipf-biased routing at T=2048 (256-row token tiles) on 64 experts (1.6 GB of
     # weights): the hardware-counter capture case of the skewed kernel shape.
     "skewed_e64": MoEConfig("skewed_e64", T=2048, D=4096, E=64, I=1024, Is=1024, k=10,

@@ -22,7 +22,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 # tokens whose layer output is compared (None: all of them)
 SAMPLE = {"decode": None, "prefill": None, "skewed": 24, "w4a16": None, "w4a16_decode": None,
-          "dense_e64": 32, "w4a16_channel": None}
+          "dense_e64": 32, "w4a16_channel": None, "w4a16_dense_e64": 32}
 
 
 def hot_tail_tokens(counts, offsets, perm, k, hottest=3, tile=256):
