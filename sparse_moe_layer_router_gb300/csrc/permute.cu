@@ -159,26 +159,39 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
 // row range (device pointers row_lo, row_hi) only for *row_lo <= r < *row_hi.
 // A source row outside [0, src_rows) is clamped into it and recorded in
 // `status` (MOE_ERR_INVALID_ARG) when that is non-null.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ a,
-                                                          const int32_t* __restrict__ idx,
-                                                          int rows, int vec_per_row, int div,
-                                                          int src_rows, uint4* __restrict__ out,
-                                                          const int32_t* __restrict__ row_lo,
-                                                          const int32_t* __restrict__ row_hi,
-                                                          int* __restrict__ status) {
+// One warp per row, kGatherRowsPerBlock rows per block; each lane issues
+// eight 16-byte loads before its stores, so a block keeps 32 KB in flight.
+constexpr int kGatherRowsPerBlock = 8;
+__global__ void __launch_bounds__(32 * kGatherRowsPerBlock) gather_rows_kernel(
+    const uint4* __restrict__ a, const int32_t* __restrict__ idx, int rows, int vec_per_row,
+    int div, int src_rows, uint4* __restrict__ out, const int32_t* __restrict__ row_lo,
+    const int32_t* __restrict__ row_hi, int* __restrict__ status) {
   pdl_wait();
   pdl_trigger();
-  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kGatherRowsPerBlock + (threadIdx.x >> 5);
   if (r >= rows) return;
   if (row_lo && (r < __ldg(row_lo) || r >= __ldg(row_hi))) return;
   int src = idx[r] / div;
   if (static_cast<unsigned>(src) >= static_cast<unsigned>(src_rows)) {
-    if (threadIdx.x == 0 && status) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+    if (lane == 0 && status) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
     src = src < 0 ? 0 : src_rows - 1;
   }
-  const uint4* s = a + static_cast<size_t>(src) * vec_per_row;
-  uint4* d = out + static_cast<size_t>(r) * vec_per_row;
-  for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = __ldg(s + i);
+  const uint4* sr = a + static_cast<size_t>(src) * vec_per_row;
+  uint4* dr = out + static_cast<size_t>(r) * vec_per_row;
+  for (int i0 = 0; i0 < vec_per_row; i0 += 8 * 32) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 32 * u + lane;
+      if (i < vec_per_row) v[u] = __ldg(sr + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 32 * u + lane;
+      if (i < vec_per_row) dr[i] = v[u];
+    }
+  }
 }
 
 // Small problems in one block of 1024 threads (one launch instead of three):
@@ -365,7 +378,8 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
                                int src_rows, void* out, const int32_t* row_lo,
                                const int32_t* row_hi, int* status, cudaStream_t st) {
-  return pdl_launch(gather_rows_kernel, dim3(rows), dim3(256), 0, st,
+  const int blocks = (rows + kGatherRowsPerBlock - 1) / kGatherRowsPerBlock;
+  return pdl_launch(gather_rows_kernel, dim3(blocks), dim3(32 * kGatherRowsPerBlock), 0, st,
                     static_cast<const uint4*>(a), idx, rows, D / 8, div, src_rows,
                     static_cast<uint4*>(out), row_lo, row_hi, status);
 }
