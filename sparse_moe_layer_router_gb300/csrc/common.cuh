@@ -85,15 +85,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
   }
 }
-// Long waits off the critical path (an epilogue waiting for a whole tile):
-// sleep so the spinning warp does not take issue slots from the producers.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
-                                                volatile int* abort) {
-  return mbar_wait<true>(bar, parity, abort);
-}
-
 // Waits with only the time bound (used while unwinding after an abort).
-__device__ __forceinline__ bool mbar_wait_time_only_r(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_time_only(uint64_t* bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > kWaitLimitNs) return false;
@@ -249,10 +242,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {

@@ -136,15 +136,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Waits with only the time bound (used while unwinding after an abort).
-__device__ __forceinline__ bool mbar_wait_time_only(uint64_t* bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
-  }
-  return true;
-}
-
 __device__ __forceinline__ void record_error(const GemmParams& p, volatile int* abort_flag,
                                              int code) {
   *abort_flag = 1;

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(
       if (!ok) {
         fail();
         for (int i = 0; i < kRtStages; ++i)
-          if ((issued >> i) & 1u) mbar_wait_time_only_r(&s.full[i], (issued_ph >> i) & 1u);
+          if ((issued >> i) & 1u) mbar_wait_time_only(&s.full[i], (issued_ph >> i) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(
       }
       if (!ok) fail();
       mma_commit(&s.drain);
-      mbar_wait_time_only_r(&s.drain, 0);
+      mbar_wait_time_only(&s.drain, 0);
     }
   } else {
     // epilogue: lane quarter warp % 4 holds experts e0 + 32 * (warp % 4) + lane
