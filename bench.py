@@ -17,6 +17,8 @@ expert included) over one batch of synthetic input, through the C ABI.
             path split into its ABI calls, against the measured HBM copy peak.
   cpu_baseline  the fp64 oracle on this host's cores over the same batch (at
             most its first 1024 tokens).
+  graph_ms_per_step  the same step captured once into a CUDA graph and
+            replayed (no host launch cost).
   configs   the same measurements for the other workloads: the T=1024 prefill
             chunk (the metric's second configuration) and the skewed T=8192
             batch on the same expert weights, the tiny layer, W4A16 at T=1024
@@ -381,6 +383,25 @@ def measure(cfg, inp, args, world, rank, dev, clocks_on, hbm_peak, bf16_peak, pe
     ms_total = slowest_rank(ms_total, world, dev)
     ms_step = ms_total / args.steps
     value = job_tokens_per_s(world, cfg.T, args.steps, ms_total / 1e3)
+
+    # ---------------- the same step replayed from a CUDA graph (captured once):
+    # no host launch cost, which is what bounds the tiny layer
+    graph_ms = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    barrier()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kg = max(10, args.steps // 3)
+    g0.record()
+    for _ in range(kg):
+        graph.replay()
+    g1.record()
+    barrier()
+    check_status(B, ws, "the graph replays")
+    graph_ms = slowest_rank(g0.elapsed_time(g1), world, dev) / kg
+    del graph
     # sums of squares, logits, select, dispatch (one block up to 4096 pairs, else
     # count + scan + scatter), gather, 2 GEMMs, combine
     launches_per_step = 8 if cfg.T * cfg.k <= 4096 else 10
@@ -500,7 +521,8 @@ def measure(cfg, inp, args, world, rank, dev, clocks_on, hbm_peak, bf16_peak, pe
                          f"x{passes} passes"}
         del inputs
     del ws, y
-    return {"value": value, "ms_per_step": ms_step, "roofline": roofline, "layer": layer,
+    return {"value": value, "ms_per_step": ms_step, "graph_ms_per_step": graph_ms,
+            "roofline": roofline, "layer": layer,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps, "workload": workload_desc(cfg)}
 
@@ -583,7 +605,8 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": max(3, args.warmup),
-                "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "ms_per_step": head["ms_per_step"], "graph_ms_per_step": head["graph_ms_per_step"],
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded; random-init weights of the stated shapes)",
                 "config": base_config, "roofline": head["roofline"],

@@ -506,3 +506,33 @@ def test_route_bit_exact_at_tiny_magnitudes(sx, sw):
     host.w_router = (host.w_router.float() * 2.0 ** sw).to(torch.bfloat16)
     dev = host.to("cuda")
     check_route(cfg, host, dev)
+
+
+@pytest.mark.parametrize("name", ["hot", "wide", "w4_table", "w4c_wide"])
+def test_forward_replays_from_a_cuda_graph(name):
+    """moe_forward captured once into a CUDA graph (all its launches are on the
+    caller's stream, chained with programmatic dependent launch) and replayed
+    on new token rows copied into the captured input buffer: every replay
+    equals an eager call on the same rows bit for bit.  "wide" takes the
+    three-kernel dispatch and the 256-row tiles; the W4A16 cases the TMEM- and
+    shared-memory-restore kernels."""
+    cfg = SMALL[name] if name in SMALL else W4[name]
+    host, dev = gpu_inputs(cfg)
+    W = B.weights_struct(dev, cfg)
+    x_in = dev.x.clone()
+    y = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device="cuda")
+    ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
+    B.forward(cfg, x_in, W, y=y, ws=ws)  # first call outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        B.forward(cfg, x_in, W, y=y, ws=ws)
+    ws_eager = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
+    for seed in (11, 12, 13):
+        x_new = normal_bf16((cfg.T, cfg.D), 1.0, seed, 77, "cpu").cuda()
+        x_in.copy_(x_new)
+        graph.replay()
+        y_eager = B.forward(cfg, x_new, W, ws=ws_eager)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_eager), seed
+    assert B.get_status(ws) == B.MOE_OK and B.get_status(ws_eager) == B.MOE_OK
