@@ -257,8 +257,13 @@ int moe_permute_static(const moe_config *cfg, const int32_t *blob,
 
 /*
  * Persistent grouped GEMM over ragged expert row groups (TMA + tcgen05/TMEM)
- * [PM, R1G, R1]; see moe_gemm_args for operands.  W4A16 weights are
- * dequantised tile by tile in shared memory just ahead of the MMA [R1].
+ * [PM, R1G, R1]; see moe_gemm_args for operands.  W4A16 weights stay packed
+ * and are restored tile by tile on chip just ahead of the MMA (into tensor
+ * memory for token tiles of up to 64 rows, into shared memory for 256-row
+ * tiles) [R1].  The call first copies `offsets` (clamped into [0, T*k] and
+ * made non-decreasing) and `perm_pair` (clamped into [0, T*k)) into ws, and
+ * the kernels read those copies; a value that needed clamping is recorded as
+ * MOE_ERR_INVALID_ARG in the status word.  ws sized for MOE_ENTRY_GROUPED_GEMM.
  */
 int moe_grouped_gemm(const moe_config *cfg, const moe_gemm_args *args, void *ws,
                      size_t ws_bytes, void *stream);
