@@ -356,8 +356,11 @@ def test_forward_parity(name):
     tol_check(y_host(y), ref)
 
 
-def test_forward_deterministic_and_host_entry():
-    cfg = SMALL["hot"]
+@pytest.mark.parametrize("name", ["hot", "w4_ragged", "w4c_wide"])
+def test_forward_deterministic_and_host_entry(name):
+    """Two calls give the same bits, and moe_forward_host (host x and y, the
+    copies inside the call) gives the device entry's bits, bf16 and W4A16."""
+    cfg = SMALL[name] if name in SMALL else W4[name]
     host, dev = gpu_inputs(cfg)
     ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
     y1 = B.forward(cfg, dev.x, dev, ws=ws).clone()
