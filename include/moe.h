@@ -349,10 +349,11 @@ int moe_repack_int4(const int32_t *src, int32_t *dst, size_t n_words, int src_la
 /*
  * Device status of the calls that used `ws` since the status was last read:
  * synchronises `stream`, returns MOE_OK or the first device-side error
- * recorded (MOE_ERR_TIMEOUT when a bounded wait inside a kernel gave up), then
- * clears it.  The status is sticky: no other entry point clears it, so an
+ * recorded (MOE_ERR_TIMEOUT when a bounded wait inside a kernel gave up,
+ * MOE_ERR_INVALID_ARG when caller index data was out of range and clamped),
+ * then clears it.  The status is sticky: no other entry point clears it, so an
  * error recorded by one call is still reported after later calls succeed.  A
- * kernel that records an error stops issuing work, so any output written by a
+ * kernel whose wait gave up stops issuing work, so any output written by a
  * call since the last MOE_OK status is not to be trusted.
  */
 int moe_get_status(void *ws, void *stream);
