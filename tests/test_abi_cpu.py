@@ -185,3 +185,34 @@ def test_binding_rejects_tensors_the_kernels_would_overrun(lib):
     with pytest.raises(ValueError, match="CUDA"):
         B.grouped_gemm(cfg, B.MOE_OP_DOWN_WEIGHTED, h, off, wd, torch.empty((P, cfg.D), dtype=f32),
                        perm_pair=perm, blob=blob)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/moe.h compiles as C99 (no C++ or CUDA types in the ABI), and a
+    caller written as the README shows type-checks against it."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text('''
+#include <stddef.h>
+#include <stdio.h>
+#include "moe.h"
+int call(const void *x, void *y, const void *wr, const void *w_gu, const void *w_dn,
+         const void *ws_gu, const void *ws_dn, void *ws, void *stream) {
+  moe_config cfg = {.T = 64, .D = 4096, .E = 512, .I = 1024, .I_shared = 1024, .k = 10,
+                    .quant = MOE_QUANT_BF16, .group = 128};
+  moe_weights w = {.w_router = wr, .router_bias = NULL, .w_gate_up = w_gu, .w_down = w_dn,
+                   .ws_gate_up = ws_gu, .ws_down = ws_dn};
+  size_t ws_bytes = moe_workspace_size(&cfg, MOE_ENTRY_FORWARD);
+  int rc = moe_forward(&cfg, x, &w, y, ws, ws_bytes, stream);
+  if (rc != MOE_OK) fprintf(stderr, "%s\\n", moe_strerror(rc));
+  return rc != MOE_OK ? rc : moe_get_status(ws, stream);
+}
+''')
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
