@@ -402,9 +402,7 @@ def measure(cfg, inp, args, world, rank, dev, clocks_on, hbm_peak, bf16_peak, pe
     check_status(B, ws, "the graph replays")
     graph_ms = slowest_rank(g0.elapsed_time(g1), world, dev) / kg
     del graph
-    # sums of squares, logits, select, dispatch (one block up to 4096 pairs, else
-    # count + scan + scatter), gather, 2 GEMMs, combine
-    launches_per_step = 8 if cfg.T * cfg.k <= 4096 else 10
+    launches_per_step = step_launches(cfg)
 
     # ---------------- the path split into its ABI calls, events around each call
     blob = torch.empty((cfg.T, 2, cfg.k), dtype=torch.int32, device=dev)
@@ -525,6 +523,19 @@ def measure(cfg, inp, args, world, rank, dev, clocks_on, hbm_peak, bf16_peak, pe
             "roofline": roofline, "layer": layer,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps, "workload": workload_desc(cfg)}
+
+
+def step_launches(cfg):
+    """Kernel launches of one moe_forward: sums of squares, logits, select,
+    dispatch (one block up to 4096 pairs, else count + scan + scatter), gather,
+    two GEMMs, combine.  A bf16 GEMM with 256-row token tiles and under 512 rows
+    per expert on average adds a plan kernel and a second grid (the hot/cold
+    split)."""
+    n = 8 if cfg.T * cfg.k <= 4096 else 10
+    tiles256 = cfg.T >= 2048 or cfg.T * cfg.k >= 48 * cfg.E
+    if cfg.quant == 0 and tiles256 and cfg.T * cfg.k < 512 * cfg.E:
+        n += 4
+    return n
 
 
 def measure_extra(names, inp, args, world, rank, dev, hbm_peak, bf16_peak, peak_src):

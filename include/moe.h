@@ -36,6 +36,13 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  Buffers must stay alive until the stream has passed the call.
  *   - Concurrent calls that share a workspace race; give each stream its own.
+ *   - A bf16 grouped GEMM with 256-row token tiles (T >= 2048 or T*k >= 48*E)
+ *     and under 512 rows per expert on average (T*k < 512*E) runs its groups
+ *     of fewer than 64 rows in a second grid on a stream of the library's,
+ *     forked from `stream` and joined back to it with events inside the call:
+ *     the call stays ordered on `stream` and can be captured into a CUDA
+ *     graph.  The stream and events are created on first use, one set per
+ *     host thread and CUDA context, and kept.
  *   - Return 0 on success or a negative MOE_ERR_* code.  Argument and shape
  *     errors are detected on the host and launch nothing.  Device-side wait
  *     timeouts are reported through moe_get_status().

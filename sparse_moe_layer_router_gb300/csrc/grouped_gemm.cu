@@ -92,6 +92,7 @@ struct GemmCommon {
   int tile_start[kMaxGroups + 1];
   int off[kMaxGroups];
   float row_weight[8][BN_MAX];  // down epilogue: routing weight of each token row, per warp
+  int walk_ctas;                // bf16 kernel: CTAs that share the tile walk
 };
 
 template <int BN_MAX, int STAGES>
@@ -224,16 +225,19 @@ __device__ __forceinline__ uint4 restore_word(uint32_t w, __nv_bfloat162 s2, boo
 }
 
 // Group table: s.off <- offsets, s.tile_start <- exclusive scan of tiles per
-// group; returns the number of tiles.  All threads of the CTA call it.
-template <int BN_MAX>
-__device__ int build_tile_table(GemmCommon<BN_MAX>& s, const GemmParams& p, int G, int nthreads) {
+// group; returns the number of tiles.  All threads of the CTA call it.  With
+// kFilter, groups whose row count lies outside [min_rows, max_rows] get none.
+template <int BN_MAX, bool kFilter = false>
+__device__ int build_tile_table(GemmCommon<BN_MAX>& s, const GemmParams& p, int G, int nthreads,
+                                int min_rows = 0, int max_rows = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i <= p.E; i += nthreads) s.off[i] = p.offsets[i];
   __syncthreads();
   for (int g = threadIdx.x; g < G; g += nthreads) {
     const bool sh = p.has_shared && g == 0;
     const int e = g - p.has_shared;
-    const int rows = sh ? p.T_shared : s.off[e + 1] - s.off[e];
+    int rows = sh ? p.T_shared : s.off[e + 1] - s.off[e];
+    if (kFilter && (rows < min_rows || rows > max_rows)) rows = 0;
     s.tile_start[g + 1] = ((rows + BN_MAX - 1) / BN_MAX) * (sh ? p.m_tiles_s : p.m_tiles);
   }
   __syncthreads();
@@ -284,7 +288,9 @@ __device__ void epilogue_role(GemmCommon<BN_MAX>& s, const GemmParams& p, int G,
   float* wts = s.row_weight[warp - 2];
   int acc = 0;
   uint32_t acc_phase = 0;
-  for (int L = blockIdx.x; L < ntiles; L += gridDim.x) {
+  // the bf16 kernel's walk may be a share of the grid (split launches)
+  const int step = NE == 8 ? s.walk_ctas : static_cast<int>(gridDim.x);
+  for (int L = blockIdx.x; L < ntiles; L += step) {
     const TileInfo t = decode_tile<BN_MAX>(s, p, G, L);
     if (p.op == kOpDown) {
       // Routing weight of every token row of the tile, fetched before the
@@ -442,6 +448,60 @@ __device__ __forceinline__ void load_token_tile(uint8_t* dst, const CUtensorMap*
 // ==========================================================================
 // bf16 weights
 // ==========================================================================
+// A split bf16 launch runs the groups of at least kSplitRows rows (tensor-bound
+// at 256-row tiles) on the first gh CTAs of one grid and the smaller groups
+// (bound by streaming their weights) on the last grid - gh CTAs of another,
+// each grid the size of the device, concurrently.  gh shares the SMs in
+// proportion to the hot groups' MMA flops and the cold groups' weight bytes,
+// the bytes weighted by kSplitFlopPerByte: one SM's MMA rate over its rate of
+// streaming weights through the eight-stage ring, measured (~125) and rounded
+// toward more streaming SMs, because too few of those costs more.  A one-warp
+// kernel computes gh before both launches (kept out of the GEMM kernel, whose
+// code generation this floating-point work upset) and both read it.
+constexpr double kSplitFlopPerByte = 140.0;
+
+__device__ __forceinline__ int split_hot_ctas(const GemmParams& p, int ncta) {
+  const int lane = threadIdx.x & 31;
+  double hot_rows = 0.0, cold_groups = 0.0;
+  for (int e = lane; e < p.E; e += 32) {
+    const int r = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    if (r >= kSplitRows)
+      hot_rows += r;
+    else if (r > 0)
+      cold_groups += 1.0;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    hot_rows += __shfl_xor_sync(0xffffffffu, hot_rows, o);
+    cold_groups += __shfl_xor_sync(0xffffffffu, cold_groups, o);
+  }
+  const double w_elems = static_cast<double>(p.m_tiles) * kBM * p.k_blocks * kBK;
+  double hot = hot_rows * 2.0 * w_elems;      // MMA flops of the hot routed rows
+  double cold = cold_groups * 2.0 * w_elems;  // bf16 weight bytes of the cold groups
+  if (p.has_shared) {
+    const double ws_elems = static_cast<double>(p.m_tiles_s) * kBM * p.k_blocks_s * kBK;
+    if (p.T_shared >= kSplitRows)
+      hot += p.T_shared * 2.0 * ws_elems;
+    else if (p.T_shared > 0)
+      cold += 2.0 * ws_elems;
+  }
+  if (cold == 0.0) return ncta;
+  if (hot == 0.0) return 0;
+  const int gh = static_cast<int>(ncta * hot / (hot + kSplitFlopPerByte * cold) + 0.5);
+  return min(max(gh, 1), ncta - 1);
+}
+
+__global__ void __launch_bounds__(32) split_plan_kernel(const GemmParams p, int ncta, int* gh) {
+  pdl_wait();
+  pdl_trigger();
+  const int v = split_hot_ctas(p, ncta);
+  if (threadIdx.x == 0) *gh = v;
+}
+
+cudaError_t launch_split_plan(const GemmParams& p, int ncta, int* gh, cudaStream_t st) {
+  return pdl_launch(split_plan_kernel, dim3(1), dim3(32), 0, st, p, ncta, gh);
+}
+
 template <int BN_MAX, int STAGES>
 __global__ void __launch_bounds__(kBf16Threads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -455,6 +515,25 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                         const __grid_constant__ CUtensorMap tm_b8,
                         const __grid_constant__ CUtensorMap tm_b8_s, const GemmParams p) {
   pdl_wait();
+  // Split launches: this grid's share of the SMs and of the groups; the CTAs
+  // beyond the share leave before taking any resource.
+  int ncta = static_cast<int>(gridDim.x);
+  int min_rows = 0, max_rows = 0x7fffffff;
+  if (p.split_role != 0) {
+    const int gh = __ldg(p.split_gh);
+    if (p.split_role == 1) {
+      ncta = gh;
+      min_rows = kSplitRows;
+    } else {
+      ncta -= gh;
+      min_rows = 1;
+      max_rows = kSplitRows - 1;
+    }
+    if (static_cast<int>(blockIdx.x) >= ncta) {
+      pdl_trigger();
+      return;
+    }
+  }
   extern __shared__ uint8_t smem_raw[];
   using Smem = Bf16Smem<BN_MAX, STAGES>;
   const uint32_t raw = smem_u32(smem_raw);
@@ -471,6 +550,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
       mbar_init(&s.empty[i], 1);
     }
     init_common_barriers<BN_MAX>(cm, kBf16EpiWarps);
+    cm.walk_ctas = ncta;
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -487,7 +567,8 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
       prefetch_tmap(&tm_b8_s);
     }
   }
-  const int ntiles = build_tile_table<BN_MAX>(cm, p, G, kBf16Threads);
+  const int ntiles =
+      build_tile_table<BN_MAX, true>(cm, p, G, kBf16Threads, min_rows, max_rows);
   if (warp == 1) {
     tmem_alloc(&cm.tmem_base, kTmemCols);
     tmem_relinquish();
@@ -511,7 +592,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
       uint32_t issued = 0;  // bit i: stage i had a load issued; its phase in issued_ph
       uint32_t issued_ph = 0;
       bool ok = true;
-      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+      for (int L = blockIdx.x; L < ntiles && ok; L += ncta) {
         const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
         const CUtensorMap* ma = t.shared ? &tm_a_s : &tm_a;
         const CUtensorMap* const mb[4] = {t.shared ? &tm_b_s : &tm_b, t.shared ? &tm_b2_s : &tm_b2,
@@ -553,7 +634,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+      for (int L = blockIdx.x; L < ntiles && ok; L += ncta) {
         const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
         if (!mbar_wait<true>(&cm.tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/moe.h"
 #include "kernels.h"
@@ -350,6 +351,75 @@ int choose_bn_max(const moe_config* c) {
   return (c->T >= 2048 || avg >= 48.0) ? 256 : 64;
 }
 
+// The second stream of split bf16 launches, with the events that fork it from
+// and join it back to the caller's stream: one set per host thread and
+// context, created on first use (in relaxed capture mode, so that a first use
+// inside a stream capture is legal) and kept for the process.
+struct SideStream {
+  unsigned long long ctx;
+  cudaStream_t stream;
+  cudaEvent_t fork, join;
+};
+thread_local std::vector<SideStream> t_side_streams;
+
+int side_stream(SideStream* out) {
+  unsigned long long id = 0;
+  if (current_context_id(&id) != cudaSuccess) return MOE_ERR_CUDA;
+  for (const SideStream& x : t_side_streams)
+    if (x.ctx == id) {
+      *out = x;
+      return MOE_OK;
+    }
+  SideStream x{id, nullptr, nullptr, nullptr};
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool ok = cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) == cudaSuccess;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess || !ok) return MOE_ERR_CUDA;
+  t_side_streams.push_back(x);
+  *out = x;
+  return MOE_OK;
+}
+
+// Whether a launch takes the split below: bf16 with 256-row tiles and few
+// enough rows per expert on average (under 8 * kSplitRows) that groups below
+// kSplitRows rows are likely.  When every group is hot the split only adds its
+// plan kernel and the fork and join (about 10 us per launch, measured at
+// T = 8192 on 512 experts), so the dense shapes keep the single launch.
+bool use_split(const moe_config* c, int bn_max) {
+  return c->quant == MOE_QUANT_BF16 && bn_max == 256 &&
+         static_cast<long>(c->T) * c->k < 8L * kSplitRows * c->E;
+}
+
+// A bf16 launch with 256-row tiles as two concurrent grids: groups of at least
+// kSplitRows rows (tensor-bound) on the caller's stream, the smaller ones
+// (weight-stream-bound, 64-row tiles and the deeper ring) on the side stream;
+// the kernels share the SMs between them on the device.
+// gh: a device int for the plan (bytes 12..15 of the workspace header).
+int launch_split(GemmParams p, const GemmMaps& maps, const DevInfo& dev, int* gh,
+                 cudaStream_t st) {
+  SideStream ss;
+  int rc = side_stream(&ss);
+  if (rc) return rc;
+  p.split_gh = gh;
+  rc = cuda_rc(launch_split_plan(p, dev.sms, gh, st));
+  if (rc) return rc;
+  if (cudaEventRecord(ss.fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(ss.stream, ss.fork, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  p.split_role = 1;
+  rc = cuda_rc(launch_grouped_gemm(p, maps, 256, MOE_QUANT_BF16, dev.sms, st));
+  if (rc) return rc;
+  p.split_role = 2;
+  rc = cuda_rc(launch_grouped_gemm(p, maps, 64, MOE_QUANT_BF16, dev.sms, ss.stream));
+  if (rc) return rc;
+  if (cudaEventRecord(ss.join, ss.stream) != cudaSuccess ||
+      cudaStreamWaitEvent(st, ss.join, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 // One grouped GEMM launch over `n_groups` routed groups (a->offsets holds
 // n_groups + 1 row offsets; a->w holds n_groups experts) plus, when
 // a->a_shared is set, a shared group of `t_shared` rows.
@@ -468,6 +538,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   if (w4 || !has_shared) maps.b2_s = maps.b4_s = maps.b8_s = maps.b_s;
   if (!p.scale_table || !has_shared) maps.sc_s = maps.a_s;
   if (!p.scale_table) maps.sc = maps.a;
+  if (use_split(c, bn_max)) return launch_split(p, maps, dev, at<int>(ws, 12), st);
   return cuda_rc(launch_grouped_gemm(p, maps, bn_max, c->quant, dev.sms, st));
 }
 

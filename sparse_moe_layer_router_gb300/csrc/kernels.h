@@ -71,6 +71,9 @@ cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int 
 cudaError_t launch_sanitize_gemm_indices(const int32_t* offsets, int n_offsets, int rows,
                                          int32_t* offsets_out, const int32_t* perm_pair,
                                          int32_t* perm_out, int* status, cudaStream_t st);
+// Unique ID of the CUDA context current on this thread (binding the primary
+// context if none is), never reused within the process.
+cudaError_t current_context_id(unsigned long long* id);
 // Capacity (int32 entries) of the fixed device array behind moe_permute_static.
 constexpr long kStaticPermuteScratchInts = 65536;
 cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int32_t* counts,
@@ -125,7 +128,16 @@ struct GemmParams {
   int group;
   int scale_table;          // W4A16: tile scales come from tm_sc / tm_sc_s by TMA
   int channel;              // W4A16: one scale per weight row ([rows]), applied in the epilogue
+  int split_role;           // bf16 kernel: 0 = every group; 1 = groups of >= kSplitRows rows on
+                            // the first gh CTAs; 2 = smaller groups on the last grid - gh
+  const int* split_gh;      // gh, written by launch_split_plan before the split launches
 };
+
+// Groups of at least this many rows count as hot (compute-bound) when a bf16
+// launch is split into a hot and a cold part.
+constexpr int kSplitRows = 64;
+// *gh <- the SMs (of ncta) that the hot part of a split launch of p gets.
+cudaError_t launch_split_plan(const GemmParams& p, int ncta, int* gh, cudaStream_t st);
 
 struct GemmMaps {
   CUtensorMap a, a_s, b, b_s;  // weights (routed, shared), activations (routed, shared)

@@ -442,6 +442,11 @@ cudaError_t current_ctx_id(unsigned long long* id) {
 }
 }  // namespace
 
+cudaError_t current_context_id(unsigned long long* id) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  return current_ctx_id(id);
+}
+
 // Device address of g_permute_scratch in the current context.  In host code
 // the symbol names a host-side stand-in, so the address is looked up with the
 // runtime (once per context, with that context current) and cached.

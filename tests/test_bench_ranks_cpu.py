@@ -69,3 +69,16 @@ def test_extra_workloads_exist_and_share_weights_where_bench_reuses_them():
         assert torch.equal(getattr(a, f), getattr(b, f)), f
     with pytest.raises(ValueError):
         with_tokens(make_inputs(base), base.with_(name="tiny_e8", E=8))
+
+
+def test_step_launch_count_follows_the_dispatch_and_split_rules():
+    """One block of dispatch up to 4096 (token, slot) pairs, else three; the
+    hot/cold split (bf16, 256-row tiles, under 512 rows per expert) adds a plan
+    kernel and a second grid to each of the two GEMMs."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from sparse_moe_layer_router_gb300.synthetic import CONFIGS
+    want = {"decode": 8, "prefill": 10, "skewed": 14, "w4a16": 10, "dense_e64": 10,
+            "w4a16_dense_e64": 10, "skewed_e64": 14, "tiny": 8}
+    for name, n in want.items():
+        assert bench.step_launches(CONFIGS[name]) == n, name

@@ -23,6 +23,9 @@ CASES = {
     # hot experts and empty experts (Zipf-biased router), 256-row token tiles
     "ep_hot": MoEConfig("ep_hot", T=2100, D=256, E=16, I=64, Is=64, k=2, zipf_s=1.2,
                         zipf_alpha=3.0),
+    # T >= 2048: the split bf16 launch (hot and cold grids) inside each range
+    "ep_split": MoEConfig("ep_split", T=2100, D=256, E=64, I=64, Is=64, k=4, zipf_s=1.2,
+                          zipf_alpha=0.3),
     "ep_w4": MoEConfig("ep_w4", T=64, D=512, E=10, I=256, Is=256, k=3, quant=1),
     "ep_w4_channel": MoEConfig("ep_w4_channel", T=64, D=512, E=10, I=256, Is=256, k=3,
                                quant=1, group=0),

@@ -36,6 +36,10 @@ SMALL = {
     # top-1 routing (weight 1), and a single routed expert
     "top1": MoEConfig("top1", T=50, D=256, E=8, I=128, Is=128, k=1),
     "single_expert": MoEConfig("single_expert", T=20, D=128, E=1, I=64, Is=64, k=1),
+    # T >= 2048 with a Zipf bias: 15 experts of >= 64 rows and 42 smaller ones, so
+    # the split bf16 launch runs both its hot and its cold grid
+    "split": MoEConfig("split", T=2100, D=256, E=64, I=64, Is=64, k=4, zipf_s=1.2,
+                       zipf_alpha=0.3),
 }
 
 # W4A16: symmetric int4 weights, group 128 along K, bf16 scales
@@ -511,14 +515,15 @@ def test_route_bit_exact_at_tiny_magnitudes(sx, sw):
     check_route(cfg, host, dev)
 
 
-@pytest.mark.parametrize("name", ["hot", "wide", "w4_table", "w4c_wide"])
+@pytest.mark.parametrize("name", ["hot", "wide", "split", "w4_table", "w4c_wide"])
 def test_forward_replays_from_a_cuda_graph(name):
-    """moe_forward captured once into a CUDA graph (all its launches are on the
-    caller's stream, chained with programmatic dependent launch) and replayed
+    """moe_forward captured once into a CUDA graph (its launches chained with
+    programmatic dependent launch on the caller's stream) and replayed
     on new token rows copied into the captured input buffer: every replay
     equals an eager call on the same rows bit for bit.  "wide" takes the
-    three-kernel dispatch and the 256-row tiles; the W4A16 cases the TMEM- and
-    shared-memory-restore kernels."""
+    three-kernel dispatch and the 256-row tiles, "split" the two grids on two
+    streams (forked from and joined to the captured stream); the W4A16 cases
+    the TMEM- and shared-memory-restore kernels."""
     cfg = SMALL[name] if name in SMALL else W4[name]
     host, dev = gpu_inputs(cfg)
     W = B.weights_struct(dev, cfg)
