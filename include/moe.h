@@ -376,6 +376,19 @@ int moe_get_status(void *ws, void *stream);
 int moe_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned int limit_ms,
                               void *stream);
 
+/*
+ * Releases what the library keeps between calls for the calling host thread
+ * in the current CUDA context: the second stream and the two events of split
+ * grouped GEMMs (see the conventions above).  Work already queued on them
+ * still completes (the CUDA runtime defers the release), so the call is safe
+ * with calls in flight.  The next split call creates them again.  Nothing
+ * else is cached across calls except moe_permute_static's address of its
+ * fixed array (a few bytes per context, kept for the process).
+ * Returns MOE_OK, or MOE_ERR_CUDA if no context could be made current or a
+ * destroy call failed.
+ */
+int moe_release_cache(void);
+
 /* Static description of an error code. */
 const char *moe_strerror(int code);
 

@@ -42,7 +42,7 @@ MOE_INT4_SEQUENTIAL_OFFSET8 = 1
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_router_logits", "moe_permute", "moe_permute_static",
            "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host",
            "moe_forward_experts", "moe_repack_int4", "moe_get_status",
-           "moe_selftest_wait_timeout", "moe_strerror")
+           "moe_selftest_wait_timeout", "moe_release_cache", "moe_strerror")
 
 
 class MoeError(RuntimeError):
@@ -99,12 +99,13 @@ def lib():
             L.moe_repack_int4.argtypes = [P, P, S, I, P]
             L.moe_get_status.argtypes = [P, P]
             L.moe_selftest_wait_timeout.argtypes = [P, S, ctypes.c_uint, P]
+            L.moe_release_cache.argtypes = []
             L.moe_strerror.argtypes = [I]
             L.moe_strerror.restype = ctypes.c_char_p
             for n in ("moe_route", "moe_router_logits", "moe_permute", "moe_permute_static",
                       "moe_grouped_gemm", "moe_combine", "moe_forward", "moe_forward_host",
                       "moe_forward_experts", "moe_repack_int4", "moe_get_status",
-                      "moe_selftest_wait_timeout"):
+                      "moe_selftest_wait_timeout", "moe_release_cache"):
                 getattr(L, n).restype = I
             _lib = L
     return _lib
@@ -387,6 +388,11 @@ def repack_int4(src, dst=None, layout=MOE_INT4_SEQUENTIAL, stream=None):
 
 def get_status(ws, stream=None) -> int:
     return int(lib().moe_get_status(_p(ws), _stream(stream)))
+
+
+def release_cache() -> None:
+    """moe_release_cache: drop this thread's cached split stream and events."""
+    _check(lib().moe_release_cache(), "moe_release_cache")
 
 
 def selftest_wait_timeout(ws, limit_ms=200, stream=None, read_status=True):

@@ -362,6 +362,25 @@ struct SideStream {
 };
 thread_local std::vector<SideStream> t_side_streams;
 
+// Destroys this thread's set for the current context (moe_release_cache).
+int release_side_streams() {
+  unsigned long long id = 0;
+  if (current_context_id(&id) != cudaSuccess) return MOE_ERR_CUDA;
+  int rc = MOE_OK;
+  for (size_t i = 0; i < t_side_streams.size();) {
+    const SideStream& x = t_side_streams[i];
+    if (x.ctx != id) {
+      ++i;
+      continue;
+    }
+    if (cudaEventDestroy(x.fork) != cudaSuccess || cudaEventDestroy(x.join) != cudaSuccess ||
+        cudaStreamDestroy(x.stream) != cudaSuccess)
+      rc = MOE_ERR_CUDA;
+    t_side_streams.erase(t_side_streams.begin() + static_cast<long>(i));
+  }
+  return rc;
+}
+
 int side_stream(SideStream* out) {
   unsigned long long id = 0;
   if (current_context_id(&id) != cudaSuccess) return MOE_ERR_CUDA;
@@ -914,6 +933,8 @@ int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned int limit_ms, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return cuda_rc(launch_selftest_wait(at<int>(ws, 0), 1000000ull * limit_ms, st));
 }
+
+int moe_release_cache(void) { return release_side_streams(); }
 
 const char* moe_strerror(int code) {
   switch (code) {

@@ -159,3 +159,20 @@ def test_first_split_call_inside_a_capture(inputs):
     assert not t.is_alive()
     assert "error" not in out, out.get("error")
     assert out["same"] == [True, True] and out["status"] == B.MOE_OK
+
+
+def test_release_cache_between_split_calls(inputs):
+    """moe_release_cache drops the calling thread's split stream and events,
+    also with a forward still queued; the next forward creates them again and
+    gives the same bits."""
+    host, dev = inputs
+    W = B.weights_struct(dev, CFG)
+    ws = B.workspace(CFG, B.MOE_ENTRY_FORWARD)
+    y0 = B.forward(CFG, dev.x, W, ws=ws)
+    B.release_cache()  # the forward may still be running
+    y1 = B.forward(CFG, dev.x, W, ws=ws)
+    B.release_cache()
+    B.release_cache()  # nothing cached: still fine
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    assert B.get_status(ws) == B.MOE_OK
