@@ -296,8 +296,11 @@ int moe_forward(const moe_config *cfg, const void *x, const moe_weights *w,
 
 /*
  * moe_forward with HOST x and y (pinned memory recommended): copies x into the
- * workspace, runs the layer, copies y back, all on `stream`.  The caller
- * synchronises the stream before reading y.
+ * workspace, runs the layer, copies y back, all ordered on `stream`.  From
+ * T >= 512 the combine runs in chunks of tokens and each chunk's copy to the
+ * host goes on the library's second stream (forked from and joined back to
+ * `stream`), overlapping the combine of the next chunk.  The caller
+ * synchronises `stream` before reading y.
  */
 int moe_forward_host(const moe_config *cfg, const void *x_host,
                      const moe_weights *w, void *y_host, void *ws,

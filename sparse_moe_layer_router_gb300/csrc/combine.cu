@@ -16,7 +16,7 @@ namespace moe {
 
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ o,
                                                       const float4* __restrict__ o_shared,
-                                                      const int32_t* __restrict__ inv_row, int T,
+                                                      const int32_t* __restrict__ inv_row, int P,
                                                       int D4, int k, uint2* __restrict__ y) {
   pdl_wait();
   pdl_trigger();
@@ -26,9 +26,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   float4 acc = o_shared ? __ldg(o_shared + static_cast<size_t>(t) * D4 + c)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
   const int32_t* rows = inv_row + static_cast<size_t>(t) * k;
-  const int P = T * k;
   for (int j = 0; j < k; ++j) {
-    // a row outside [0, T*k) (an inv_row that moe_permute did not write) is
+    // a row outside [0, P) (an inv_row that moe_permute did not write) is
     // clamped, so the load stays inside o
     const int r = min(max(__ldg(rows + j), 0), P - 1);
     const float4 v = __ldg(o + static_cast<size_t>(r) * D4 + c);
@@ -46,11 +45,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
 }
 
 cudaError_t launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T,
-                           int D, int k, void* y, cudaStream_t st) {
+                           int P, int D, int k, void* y, cudaStream_t st) {
   const int D4 = D / 4;
   dim3 grid(T, (D4 + 255) / 256);
   return pdl_launch(combine_kernel, grid, dim3(256), 0, st, reinterpret_cast<const float4*>(o),
-                    reinterpret_cast<const float4*>(o_shared), inv_row, T, D4, k,
+                    reinterpret_cast<const float4*>(o_shared), inv_row, P, D4, k,
                     static_cast<uint2*>(y));
 }
 

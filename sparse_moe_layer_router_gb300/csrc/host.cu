@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -591,8 +592,10 @@ int check_weights(const moe_config* c, const moe_weights* w) {
   return MOE_OK;
 }
 
+// The whole layer on `st`; with combine = false it stops after the down GEMM
+// (o and o_shared in ws) and y is not written.
 int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const moe_weights* w,
-                 void* y, void* ws, const Layout& L, cudaStream_t st) {
+                 void* y, void* ws, const Layout& L, cudaStream_t st, bool combine = true) {
   int rc = route_impl(c, dev, x, w->w_router, w->router_bias, at<int32_t>(ws, L.blob), ws, L, st);
   if (rc) return rc;
   rc = cuda_rc(launch_permute(at<int32_t>(ws, L.blob), c->T, c->k, c->E, at<int32_t>(ws, L.chunk),
@@ -630,9 +633,48 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   d.ws_scales = w->ss_down;
   d.out_shared = at<void>(ws, L.os);
   rc = gemm_impl(c, dev, &d, ws, L, st, nullptr, c->E, c->T);
-  if (rc) return rc;
+  if (rc || !combine) return rc;
   return cuda_rc(launch_combine(at<float>(ws, L.o), at<float>(ws, L.os), at<int32_t>(ws, L.inv),
-                                c->T, c->D, c->k, y, st));
+                                c->T, c->T * c->k, c->D, c->k, y, st));
+}
+
+// moe_forward_host's last step: the combine in chunks of tokens, each chunk's
+// copy to the host queued on the library's second stream as soon as the
+// chunk is combined, so that the copies (bound by the host link) overlap the
+// combine of the chunks after them.  Chunks of at least 256 tokens, at most 8.
+int combine_to_host(const moe_config* c, void* ws, const Layout& L, void* y_dev, void* y_host,
+                    cudaStream_t st) {
+  const int P = c->T * c->k;
+  const size_t row = static_cast<size_t>(c->D) * 2;
+  const int nc = std::max(1, std::min(8, c->T / 256));
+  if (nc == 1) {
+    const int rc = cuda_rc(launch_combine(at<float>(ws, L.o), at<float>(ws, L.os),
+                                          at<int32_t>(ws, L.inv), c->T, P, c->D, c->k, y_dev, st));
+    if (rc) return rc;
+    return cudaMemcpyAsync(y_host, y_dev, c->T * row, cudaMemcpyDeviceToHost, st) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  }
+  SideStream ss;
+  int rc = side_stream(&ss);
+  if (rc) return rc;
+  const int tc = (c->T + nc - 1) / nc;
+  for (int t0 = 0; t0 < c->T; t0 += tc) {
+    const int n = std::min(tc, c->T - t0);
+    rc = cuda_rc(launch_combine(at<float>(ws, L.o), at<float>(ws, L.os) + static_cast<size_t>(t0) * c->D,
+                                at<int32_t>(ws, L.inv) + static_cast<size_t>(t0) * c->k, n, P, c->D,
+                                c->k, static_cast<char*>(y_dev) + t0 * row, st));
+    if (rc) return rc;
+    if (cudaEventRecord(ss.fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(ss.stream, ss.fork, 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<char*>(y_host) + t0 * row, static_cast<char*>(y_dev) + t0 * row,
+                        n * row, cudaMemcpyDeviceToHost, ss.stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (cudaEventRecord(ss.join, ss.stream) != cudaSuccess ||
+      cudaStreamWaitEvent(st, ss.join, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 // Expert-parallel slice: dispatch every pair, but gather, compute and combine
@@ -820,8 +862,8 @@ int moe_combine(const moe_config* cfg, const float* o, const float* o_shared,
   DevInfo dev;
   rc = current_device(&dev);
   if (rc) return rc;
-  return cuda_rc(launch_combine(o, o_shared, inv_row, cfg->T, cfg->D, cfg->k, y,
-                                static_cast<cudaStream_t>(stream)));
+  return cuda_rc(launch_combine(o, o_shared, inv_row, cfg->T, cfg->T * cfg->k, cfg->D, cfg->k,
+                                y, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* y, void* ws,
@@ -858,11 +900,9 @@ int moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weight
   void* yd = at<void>(ws, L.yout);
   if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  rc = forward_impl(cfg, dev, xd, w, yd, ws, L, st);
+  rc = forward_impl(cfg, dev, xd, w, yd, ws, L, st, false);
   if (rc) return rc;
-  if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return combine_to_host(cfg, ws, L, yd, y_host, st);
 }
 
 int moe_forward_experts(const moe_config* cfg, const void* x, const int32_t* blob,

@@ -81,8 +81,10 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
                                   const void* x, int D, void* x_perm, cudaStream_t st);
 
 // ---- combine (combine.cu)
+// Tokens [0, T) of inv_row / o_shared / y (offset pointers give a token
+// range); o has P rows (inv_row values are clamped into [0, P)).
 cudaError_t launch_combine(const float* o, const float* o_shared, const int32_t* inv_row, int T,
-                           int D, int k, void* y, cudaStream_t st);
+                           int P, int D, int k, void* y, cudaStream_t st);
 
 // Expert-parallel slice: y32[t] = (s0 <= t < s1 ? o_shared[t - s0] : 0)
 //   + sum_j (*row_lo <= inv_row[t*k+j] < *row_hi ? o[inv_row[t*k+j]] : 0), fp32 out.

@@ -360,10 +360,14 @@ def test_forward_parity(name):
     tol_check(y_host(y), ref)
 
 
-@pytest.mark.parametrize("name", ["hot", "w4_ragged", "w4c_wide"])
-def test_forward_deterministic_and_host_entry(name):
+@pytest.mark.parametrize("name,pinned", [("hot", True), ("wide", True), ("wide", False),
+                                         ("split", True), ("w4_ragged", True), ("w4c_wide", True)])
+def test_forward_deterministic_and_host_entry(name, pinned):
     """Two calls give the same bits, and moe_forward_host (host x and y, the
-    copies inside the call) gives the device entry's bits, bf16 and W4A16."""
+    copies inside the call) gives the device entry's bits, bf16 and W4A16.
+    "wide" and "split" (T = 2100) take the chunked combine whose copies to the
+    host overlap it (eight chunks, the last one shorter), also with pageable
+    host buffers."""
     cfg = SMALL[name] if name in SMALL else W4[name]
     host, dev = gpu_inputs(cfg)
     ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
@@ -371,11 +375,16 @@ def test_forward_deterministic_and_host_entry(name):
     y2 = B.forward(cfg, dev.x, dev, ws=ws).clone()
     assert torch.equal(y1, y2)
     wsh = B.workspace(cfg, B.MOE_ENTRY_FORWARD_HOST)
-    xh = host.x.clone().pin_memory()
-    yh = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16).pin_memory()
-    B.forward_host(cfg, xh, dev, yh, wsh)
-    torch.cuda.synchronize()
-    assert torch.equal(yh, y1.cpu())
+    xh = host.x.clone()
+    yh = torch.full((cfg.T, cfg.D), 5.0, dtype=torch.bfloat16)
+    if pinned:
+        xh, yh = xh.pin_memory(), yh.pin_memory()
+    for _ in range(2):
+        B.forward_host(cfg, xh, dev, yh, wsh)
+        torch.cuda.synchronize()
+        assert torch.equal(yh, y1.cpu())
+        yh.fill_(5.0)
+    assert B.get_status(wsh) == B.MOE_OK
 
 
 @pytest.mark.parametrize("name", list(W4))
