@@ -299,8 +299,10 @@ int moe_forward(const moe_config *cfg, const void *x, const moe_weights *w,
  * workspace, runs the layer, copies y back, all ordered on `stream`.  From
  * T >= 512 the combine runs in chunks of tokens and each chunk's copy to the
  * host goes on the library's second stream (forked from and joined back to
- * `stream`), overlapping the combine of the next chunk.  The caller
- * synchronises `stream` before reading y.
+ * `stream`), overlapping the combine of the next chunk; from T >= 4096 x is
+ * likewise copied in 2048-token chunks, each routed once it has arrived.
+ * Results equal moe_forward's bit for bit.  The caller synchronises `stream`
+ * before reading y.
  */
 int moe_forward_host(const moe_config *cfg, const void *x_host,
                      const moe_weights *w, void *y_host, void *ws,

@@ -325,26 +325,42 @@ float router_gamma2(const moe_config* c) {
   return std::nextafter(static_cast<float>(g), INFINITY);
 }
 
-int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* wr,
-               const float* bias, int32_t* blob, void* ws, const Layout& L, cudaStream_t st) {
-  const RouterPlan rp = router_plan(c);
-  // Clears the two refinement counters for this call.  The status word before
-  // them is left alone: an error recorded by an earlier call stays until
-  // moe_get_status reads it.
-  if (cudaMemsetAsync(static_cast<char*>(ws) + 4, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
+// Routes tokens [t0, t0 + n) of x into their rows of blob with the plan rp
+// (split-K shape and radius).  Tokens are routed independently, so routing a
+// batch in pieces with the whole batch's plan gives the bits of one call.
+int route_rows(const moe_config* c, const RouterPlan& rp, const void* x, int t0, int n,
+               const void* wr, const float* bias, int32_t* blob, void* ws, const Layout& L,
+               cudaStream_t st) {
+  const void* xr = static_cast<const char*>(x) + static_cast<size_t>(t0) * c->D * 2;
+  int32_t* br = blob + static_cast<size_t>(t0) * 2 * c->k;
   float* zpart = at<float>(ws, L.zpart);
   float* xsq = at<float>(ws, L.xnorm);
   float* wsq = at<float>(ws, L.wnorm);
   CUtensorMap mw, mx;
-  if (!map_2d_bf16(&mw, wr, c->E, c->D, 128) || !map_2d_bf16(&mx, x, c->T, c->D, 64))
+  if (!map_2d_bf16(&mw, wr, c->E, c->D, 128) || !map_2d_bf16(&mx, xr, n, c->D, 64))
     return MOE_ERR_CUDA;
-  const int rc = cuda_rc(launch_router_logits_tc(mw, mx, x, wr, c->T, c->D, c->E, rp.S,
+  const int rc = cuda_rc(launch_router_logits_tc(mw, mx, xr, wr, n, c->D, c->E, rp.S,
                                                  rp.kb_per_split, zpart, xsq, wsq,
                                                  at<int>(ws, 0), st));
   if (rc != MOE_OK) return rc;
-  return cuda_rc(launch_router_select(zpart, rp.S, c->T, c->D, c->E, c->k, bias, xsq, wsq,
-                                      router_gamma(c, rp), router_gamma2(c), x, wr, blob,
+  return cuda_rc(launch_router_select(zpart, rp.S, n, c->D, c->E, c->k, bias, xsq, wsq,
+                                      router_gamma(c, rp), router_gamma2(c), xr, wr, br,
                                       at<int>(ws, 4), st));
+}
+
+// Clears the two refinement counters for this call.  The status word before
+// them is left alone: an error recorded by an earlier call stays until
+// moe_get_status reads it.
+int clear_route_counters(void* ws, cudaStream_t st) {
+  return cudaMemsetAsync(static_cast<char*>(ws) + 4, 0, 8, st) == cudaSuccess ? MOE_OK
+                                                                               : MOE_ERR_CUDA;
+}
+
+int route_impl(const moe_config* c, const DevInfo&, const void* x, const void* wr,
+               const float* bias, int32_t* blob, void* ws, const Layout& L, cudaStream_t st) {
+  const int rc = clear_route_counters(ws, st);
+  if (rc) return rc;
+  return route_rows(c, router_plan(c), x, 0, c->T, wr, bias, blob, ws, L, st);
 }
 
 int choose_bn_max(const moe_config* c) {
@@ -592,12 +608,17 @@ int check_weights(const moe_config* c, const moe_weights* w) {
   return MOE_OK;
 }
 
-// The whole layer on `st`; with combine = false it stops after the down GEMM
-// (o and o_shared in ws) and y is not written.
+// The whole layer on `st`; with route = false the blob in ws is already
+// written, and with combine = false it stops after the down GEMM (o and
+// o_shared in ws) and y is not written.
 int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const moe_weights* w,
-                 void* y, void* ws, const Layout& L, cudaStream_t st, bool combine = true) {
-  int rc = route_impl(c, dev, x, w->w_router, w->router_bias, at<int32_t>(ws, L.blob), ws, L, st);
-  if (rc) return rc;
+                 void* y, void* ws, const Layout& L, cudaStream_t st, bool combine = true,
+                 bool route = true) {
+  int rc = MOE_OK;
+  if (route) {
+    rc = route_impl(c, dev, x, w->w_router, w->router_bias, at<int32_t>(ws, L.blob), ws, L, st);
+    if (rc) return rc;
+  }
   rc = cuda_rc(launch_permute(at<int32_t>(ws, L.blob), c->T, c->k, c->E, at<int32_t>(ws, L.chunk),
                               at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                               at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), at<int>(ws, 0), st));
@@ -636,6 +657,46 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   if (rc || !combine) return rc;
   return cuda_rc(launch_combine(at<float>(ws, L.o), at<float>(ws, L.os), at<int32_t>(ws, L.inv),
                                 c->T, c->T * c->k, c->D, c->k, y, st));
+}
+
+// moe_forward_host's first step: x copied into the workspace and routed.  From
+// T = 4096 the copy runs in chunks of 2048 tokens on the library's second
+// stream, and each chunk is routed on `st` once it has arrived (with the whole
+// batch's router plan), overlapping the copy of the chunks after it: the copy
+// is bound by the host link, and a 2048-token route call costs little more
+// per token than a whole batch's.
+int host_copy_and_route(const moe_config* c, const void* x_host, void* xd, const moe_weights* w,
+                        void* ws, const Layout& L, cudaStream_t st) {
+  const size_t row = static_cast<size_t>(c->D) * 2;
+  const RouterPlan rp = router_plan(c);
+  int32_t* blob = at<int32_t>(ws, L.blob);
+  int rc = clear_route_counters(ws, st);
+  if (rc) return rc;
+  constexpr int kChunk = 2048;
+  if (c->T < 2 * kChunk) {
+    if (cudaMemcpyAsync(xd, x_host, c->T * row, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return route_rows(c, rp, xd, 0, c->T, w->w_router, w->router_bias, blob, ws, L, st);
+  }
+  SideStream ss;
+  rc = side_stream(&ss);
+  if (rc) return rc;
+  // the copies start after the work already queued on `st` (it may still read ws)
+  if (cudaEventRecord(ss.fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(ss.stream, ss.fork, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int t0 = 0; t0 < c->T; t0 += kChunk) {
+    const int n = std::min(kChunk, c->T - t0);
+    if (cudaMemcpyAsync(static_cast<char*>(xd) + t0 * row,
+                        static_cast<const char*>(x_host) + t0 * row, n * row,
+                        cudaMemcpyHostToDevice, ss.stream) != cudaSuccess ||
+        cudaEventRecord(ss.join, ss.stream) != cudaSuccess ||
+        cudaStreamWaitEvent(st, ss.join, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    rc = route_rows(c, rp, xd, t0, n, w->w_router, w->router_bias, blob, ws, L, st);
+    if (rc) return rc;
+  }
+  return MOE_OK;
 }
 
 // moe_forward_host's last step: the combine in chunks of tokens, each chunk's
@@ -895,12 +956,11 @@ int moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weight
   rc = begin(cfg, MOE_ENTRY_FORWARD_HOST, ws, ws_bytes, &dev, &L);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t bytes = static_cast<size_t>(cfg->T) * cfg->D * 2;
   void* xd = at<void>(ws, L.xin);
   void* yd = at<void>(ws, L.yout);
-  if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  rc = forward_impl(cfg, dev, xd, w, yd, ws, L, st, false);
+  rc = host_copy_and_route(cfg, x_host, xd, w, ws, L, st);
+  if (rc) return rc;
+  rc = forward_impl(cfg, dev, xd, w, yd, ws, L, st, false, false);
   if (rc) return rc;
   return combine_to_host(cfg, ws, L, yd, y_host, st);
 }

@@ -360,15 +360,22 @@ def test_forward_parity(name):
     tol_check(y_host(y), ref)
 
 
+# T >= 4096: moe_forward_host copies and routes x in 2048-token chunks (the
+# last one 104 tokens, routed by the block-per-token select kernel).
+HOST_CHUNKS = MoEConfig("host_chunks", T=4200, D=256, E=32, I=64, Is=64, k=2)
+
+
 @pytest.mark.parametrize("name,pinned", [("hot", True), ("wide", True), ("wide", False),
-                                         ("split", True), ("w4_ragged", True), ("w4c_wide", True)])
+                                         ("split", True), ("host_chunks", True),
+                                         ("host_chunks", False), ("w4_ragged", True),
+                                         ("w4c_wide", True)])
 def test_forward_deterministic_and_host_entry(name, pinned):
     """Two calls give the same bits, and moe_forward_host (host x and y, the
     copies inside the call) gives the device entry's bits, bf16 and W4A16.
     "wide" and "split" (T = 2100) take the chunked combine whose copies to the
-    host overlap it (eight chunks, the last one shorter), also with pageable
-    host buffers."""
-    cfg = SMALL[name] if name in SMALL else W4[name]
+    host overlap it (eight chunks, the last one shorter); "host_chunks" also
+    routes x chunk by chunk as it arrives; pinned and pageable host buffers."""
+    cfg = HOST_CHUNKS if name == "host_chunks" else SMALL[name] if name in SMALL else W4[name]
     host, dev = gpu_inputs(cfg)
     ws = B.workspace(cfg, B.MOE_ENTRY_FORWARD)
     y1 = B.forward(cfg, dev.x, dev, ws=ws).clone()
