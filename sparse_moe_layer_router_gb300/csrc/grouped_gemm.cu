@@ -438,13 +438,6 @@ __device__ __forceinline__ void load_token_tile_p2(uint8_t* dst, const CUtensorM
   }
 }
 
-// Token tile of k-block kb: bn rows of 64 K in 16-row boxes (128-B swizzle).
-__device__ __forceinline__ void load_token_tile(uint8_t* dst, const CUtensorMap* mb, uint64_t* bar,
-                                                const TileInfo& t, int kb, uint64_t pol) {
-  for (int i = 0; i < t.bn / 16; ++i)
-    tma_load_2d(dst + i * 2048, mb, bar, kb * kBK, t.b_row + 16 * i, pol);
-}
-
 // ==========================================================================
 // bf16 weights
 // ==========================================================================
@@ -709,6 +702,12 @@ __global__ void __launch_bounds__(kW4Threads, 1)
                            const __grid_constant__ CUtensorMap tm_a_s,
                            const __grid_constant__ CUtensorMap tm_b,
                            const __grid_constant__ CUtensorMap tm_b_s,
+                           const __grid_constant__ CUtensorMap tm_b2,
+                           const __grid_constant__ CUtensorMap tm_b2_s,
+                           const __grid_constant__ CUtensorMap tm_b4,
+                           const __grid_constant__ CUtensorMap tm_b4_s,
+                           const __grid_constant__ CUtensorMap tm_b8,
+                           const __grid_constant__ CUtensorMap tm_b8_s,
                            const __grid_constant__ CUtensorMap tm_sc,
                            const __grid_constant__ CUtensorMap tm_sc_s, const GemmParams p) {
   pdl_wait();
@@ -746,10 +745,16 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   if (threadIdx.x == 32) {
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
+    prefetch_tmap(&tm_b2);
+    prefetch_tmap(&tm_b4);
+    prefetch_tmap(&tm_b8);
     if (table) prefetch_tmap(&tm_sc);
     if (p.has_shared) {
       prefetch_tmap(&tm_a_s);
       prefetch_tmap(&tm_b_s);
+      prefetch_tmap(&tm_b2_s);
+      prefetch_tmap(&tm_b4_s);
+      prefetch_tmap(&tm_b8_s);
       if (table) prefetch_tmap(&tm_sc_s);
     }
   }
@@ -886,6 +891,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   } else if (warp == kTokenWarp) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer: token tiles
+      // in power-of-two boxes of 16 to 128 rows (two copies for 256 rows).
       const uint64_t pol_x = policy_evict_last();
       int bs = 0;
       uint32_t bph = 0;
@@ -893,7 +899,9 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
         const TileInfo t = decode_tile<BN_MAX>(cm, p, G, L);
-        const CUtensorMap* mb = t.shared ? &tm_b_s : &tm_b;
+        const CUtensorMap* const mb[4] = {t.shared ? &tm_b_s : &tm_b, t.shared ? &tm_b2_s : &tm_b2,
+                                          t.shared ? &tm_b4_s : &tm_b4,
+                                          t.shared ? &tm_b8_s : &tm_b8};
         for (int kb = 0; kb < t.k_blocks; ++kb) {
           if (!mbar_wait(&s.bempty[bs], bph ^ 1u, abort_flag)) {
             ok = false;
@@ -902,7 +910,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           mbar_arrive_expect_tx(&s.bfull[bs], static_cast<uint32_t>(t.bn) * 128u);
           b_iss |= 1u << bs;
           b_issph = (b_issph & ~(1u << bs)) | (bph << bs);
-          load_token_tile(s.b[bs], mb, &s.bfull[bs], t, kb, pol_x);
+          load_token_tile_p2(s.b[bs], mb, &s.bfull[bs], t, kb, pol_x);
           if (++bs == BSTAGES) {
             bs = 0;
             bph ^= 1u;
@@ -1420,8 +1428,8 @@ static cudaError_t launch_w4(const GemmParams& p, const GemmMaps& m, int num_sms
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return pdl_launch(kern, dim3(num_sms), dim3(kW4Threads), smem, st, m.a, m.a_s, m.b, m.b_s, m.sc,
-                    m.sc_s, p);
+  return pdl_launch(kern, dim3(num_sms), dim3(kW4Threads), smem, st, m.a, m.a_s, m.b, m.b_s, m.b2,
+                    m.b2_s, m.b4, m.b4_s, m.b8, m.b8_s, m.sc, m.sc_s, p);
 }
 
 template <int PSTAGES, int TSTAGES, int ND>
@@ -1445,7 +1453,12 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, const GemmMaps& maps, int b
     if (bn_max == 256) return launch_bf16<256, 4>(p, maps, num_sms, st);
   } else if (quant == 1) {
     if (bn_max == 64) return launch_w4t<6, 3, 8>(p, maps, num_sms, st);
-    if (bn_max == 256) return launch_w4<256, 3, 2>(p, maps, num_sms, st);
+    // gate/up (64 k-blocks per tile) gains from a third token stage, which
+    // the shared memory holds with two packed stages; down (16 k-blocks per
+    // tile) keeps three packed stages.
+    if (bn_max == 256)
+      return p.op == kOpGateUp ? launch_w4<256, 2, 3>(p, maps, num_sms, st)
+                               : launch_w4<256, 3, 2>(p, maps, num_sms, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -497,8 +497,10 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
   p.channel = (w4 && c->group == 0) ? 1 : 0;
   p.group = (w4 && c->group > 0) ? c->group : 128;
   const int bn_max = choose_bn_max(c);
-  // The W4A16 64-row kernel copies token rows in 32-row boxes, the others in 16.
+  // The W4A16 64-row kernel copies token rows in 32-row boxes; the others
+  // copy a tile's rows in power-of-two boxes of 16 to 128 rows (maps b..b8).
   const uint32_t tok_rows = (w4 && bn_max == 64) ? 32 : 16;
+  const bool p2_boxes = !w4 || bn_max == 256;
   bool ok = true;
   if (gate_up) {
     p.m_tiles = c->I / 64;
@@ -510,7 +512,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     ok &= w4 ? map_gate_up_i4(&maps.a, a->w, n_groups, c->I, c->D)
              : map_gate_up_bf16_4d(&maps.a, a->w, n_groups, c->I, c->D);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->D, tok_rows);
-    if (!w4) {
+    if (p2_boxes) {
       ok &= map_2d_bf16(&maps.b2, b_routed, P, c->D, 32);
       ok &= map_2d_bf16(&maps.b4, b_routed, P, c->D, 64);
       ok &= map_2d_bf16(&maps.b8, b_routed, P, c->D, 128);
@@ -519,7 +521,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
       ok &= w4 ? map_gate_up_i4(&maps.a_s, a->w_shared, 1, c->I_shared, c->D)
                : map_gate_up_bf16_4d(&maps.a_s, a->w_shared, 1, c->I_shared, c->D);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, t_shared, c->D, tok_rows);
-      if (!w4) {
+      if (p2_boxes) {
         ok &= map_2d_bf16(&maps.b2_s, a->a_shared, t_shared, c->D, 32);
         ok &= map_2d_bf16(&maps.b4_s, a->a_shared, t_shared, c->D, 64);
         ok &= map_2d_bf16(&maps.b8_s, a->a_shared, t_shared, c->D, 128);
@@ -536,7 +538,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     ok &= w4 ? map_2d_i4(&maps.a, a->w, static_cast<uint64_t>(n_groups) * c->D, c->I, 128)
              : map_2d_bf16(&maps.a, a->w, static_cast<uint64_t>(n_groups) * c->D, c->I, 128);
     ok &= map_2d_bf16(&maps.b, b_routed, P, c->I, tok_rows);
-    if (!w4) {
+    if (p2_boxes) {
       ok &= map_2d_bf16(&maps.b2, b_routed, P, c->I, 32);
       ok &= map_2d_bf16(&maps.b4, b_routed, P, c->I, 64);
       ok &= map_2d_bf16(&maps.b8, b_routed, P, c->I, 128);
@@ -545,7 +547,7 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
       ok &= w4 ? map_2d_i4(&maps.a_s, a->w_shared, c->D, c->I_shared, 128)
                : map_2d_bf16(&maps.a_s, a->w_shared, c->D, c->I_shared, 128);
       ok &= map_2d_bf16(&maps.b_s, a->a_shared, t_shared, c->I_shared, tok_rows);
-      if (!w4) {
+      if (p2_boxes) {
         ok &= map_2d_bf16(&maps.b2_s, a->a_shared, t_shared, c->I_shared, 32);
         ok &= map_2d_bf16(&maps.b4_s, a->a_shared, t_shared, c->I_shared, 64);
         ok &= map_2d_bf16(&maps.b8_s, a->a_shared, t_shared, c->I_shared, 128);
@@ -566,12 +568,12 @@ int gemm_impl(const moe_config* c, const DevInfo& dev, const moe_gemm_args* a, v
     }
   }
   if (!ok) return MOE_ERR_CUDA;
-  if (w4) maps.b2 = maps.b4 = maps.b8 = maps.b;
+  if (!p2_boxes) maps.b2 = maps.b4 = maps.b8 = maps.b;
   if (!has_shared) {
     maps.a_s = maps.a;
     maps.b_s = maps.b;
   }
-  if (w4 || !has_shared) maps.b2_s = maps.b4_s = maps.b8_s = maps.b_s;
+  if (!p2_boxes || !has_shared) maps.b2_s = maps.b4_s = maps.b8_s = maps.b_s;
   if (!p.scale_table || !has_shared) maps.sc_s = maps.a_s;
   if (!p.scale_table) maps.sc = maps.a;
   if (use_split(c, bn_max)) return launch_split(p, maps, dev, at<int>(ws, 12), st);
