@@ -15,7 +15,8 @@
 //     with few tokens still streams full-width weight tiles.
 //   * warp 0: TMA producer (one thread); warp 1: TMEM allocation and
 //     tcgen05.mma issue (one thread), fp32 accumulators in TMEM, double
-//     buffered; warps 2-5: epilogue (tcgen05.ld).  The W4A16 kernels add
+//     buffered; warps 2-5: epilogue (tcgen05.ld; warps 2-9 in the bf16
+//     kernel, two per TMEM lane quarter).  The W4A16 kernels add
 //     dequant warps that restore the packed int4 tiles (into the shared-memory
 //     operand for 256-row token tiles, into tensor memory for tiles of up to 64
 //     rows) and a token-row producer warp; the TMEM variant has a second MMA
@@ -23,7 +24,9 @@
 //   * Tiles: every CTA walks tile indices blockIdx.x, +gridDim.x, ... over the
 //     concatenation of groups [shared, expert 0, ..., expert E-1]; a group with
 //     R rows has ceil(R / BN_MAX) * m_tiles tiles, token tiles of one weight
-//     tile adjacent so repeated weight tiles come from L2.
+//     tile adjacent so repeated weight tiles come from L2.  A split bf16
+//     launch runs as two grids, each walking only its own groups (those of
+//     at least kSplitRows rows, or the smaller ones) on its share of the SMs.
 //   * Gate/up: a tile covers 64 output features; its A rows are four blocks of
 //     (16 gate rows, 16 up rows) (one 4-D TMA box for bf16, four 3-D boxes for
 //     int4), so each epilogue warp holds gate and up of the same 16 features in
