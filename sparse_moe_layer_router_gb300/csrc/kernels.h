@@ -63,6 +63,13 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
                                int src_rows, void* out, const int32_t* row_lo,
                                const int32_t* row_hi, int* status, cudaStream_t st);
+// out[inv_row[t*k + j]] = x[t] for every token t < T and slot j < k (k <= 32):
+// the same rows as launch_gather_rows(x, perm_pair, ...) with div = k, each x
+// row read once.  Destination rows outside [0, rows) are skipped (recorded in
+// status); with row_lo / row_hi only rows in [*row_lo, *row_hi) are written.
+cudaError_t launch_scatter_rows(const void* x, const int32_t* inv_row, int T, int k, int D,
+                                int rows, void* out, const int32_t* row_lo,
+                                const int32_t* row_hi, int* status, cudaStream_t st);
 // Caller index arrays made safe for the grouped GEMM: offsets_out[i] = the
 // running maximum of offsets[0..i] clamped into [0, rows] (monotone, so every
 // group's row range lies inside [0, rows)); perm_out[r] = perm_pair[r] clamped

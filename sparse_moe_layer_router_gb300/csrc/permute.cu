@@ -194,6 +194,52 @@ __global__ void __launch_bounds__(32 * kGatherRowsPerBlock) gather_rows_kernel(
   }
 }
 
+// Token-major form of the same copy: one warp per token reads its x row once
+// and writes it to the k grouped rows inv_row[t*k + j], so each x row crosses
+// HBM once (a row-major gather reads it k times, and at large T the grouped
+// rows streaming through L2 evict x between those reads).  Destination rows
+// outside [0, rows) are skipped and recorded; with row_lo / row_hi only rows
+// in [*row_lo, *row_hi) are written.
+constexpr int kScatterTokensPerBlock = 8;
+__global__ void __launch_bounds__(32 * kScatterTokensPerBlock) scatter_rows_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ inv_row, int T, int k,
+    int vec_per_row, int rows, uint4* __restrict__ out, const int32_t* __restrict__ row_lo,
+    const int32_t* __restrict__ row_hi, int* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kScatterTokensPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lo = row_lo ? __ldg(row_lo) : 0;
+  const int hi = row_hi ? __ldg(row_hi) : rows;
+  // lane j < k holds destination j
+  int dst = lane < k ? __ldg(inv_row + static_cast<size_t>(t) * k + lane) : -1;
+  if (lane < k && static_cast<unsigned>(dst) >= static_cast<unsigned>(rows)) {
+    if (status) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+    dst = -1;
+  }
+  if (dst < lo || dst >= hi) dst = -1;
+  const uint4* sr = x + static_cast<size_t>(t) * vec_per_row;
+  for (int i0 = 0; i0 < vec_per_row; i0 += 8 * 32) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 32 * u + lane;
+      if (i < vec_per_row) v[u] = __ldg(sr + i);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, dst, j);
+      if (r < 0) continue;
+      uint4* dr = out + static_cast<size_t>(r) * vec_per_row;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + 32 * u + lane;
+        if (i < vec_per_row) dr[i] = v[u];
+      }
+    }
+  }
+}
+
 // Small problems in one block of 1024 threads (one launch instead of three):
 // warp w owns pairs [w*seg, (w+1)*seg); per-warp expert counts in shared
 // memory, one block-wide scan over experts, then each warp places its pairs
@@ -373,6 +419,15 @@ cudaError_t launch_permute(const int32_t* blob, int T, int k, int E, int32_t* ch
   if (e != cudaSuccess) return e;
   return pdl_launch(permute_scatter_kernel, dim3(B), dim3(256), smem_scatter, st, blob, P, k, E,
                     chunk_cnt, perm_pair, inv_row);
+}
+
+cudaError_t launch_scatter_rows(const void* x, const int32_t* inv_row, int T, int k, int D,
+                                int rows, void* out, const int32_t* row_lo,
+                                const int32_t* row_hi, int* status, cudaStream_t st) {
+  const int blocks = (T + kScatterTokensPerBlock - 1) / kScatterTokensPerBlock;
+  return pdl_launch(scatter_rows_kernel, dim3(blocks), dim3(32 * kScatterTokensPerBlock), 0, st,
+                    static_cast<const uint4*>(x), inv_row, T, k, D / 8, rows,
+                    static_cast<uint4*>(out), row_lo, row_hi, status);
 }
 
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
