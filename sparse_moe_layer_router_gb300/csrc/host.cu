@@ -625,17 +625,10 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
                               at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                               at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), at<int>(ws, 0), st));
   if (rc) return rc;
-  // dispatch: token rows in grouped order.  From T = 2048 each token's row is
-  // read once and written to its k grouped rows (inv_row): at T = 8192 the
-  // grouped rows (671 MB) evict x from L2 between a row-major gather's k reads
-  // of a row (skewed step -1.2%).  Below that the row gather spreads the
-  // copy over more blocks (decode: 80 blocks instead of 8; 5 us faster).
-  if (c->T >= 2048)
-    rc = cuda_rc(launch_scatter_rows(x, at<int32_t>(ws, L.inv), c->T, c->k, c->D, c->T * c->k,
-                                     at<void>(ws, L.xperm), nullptr, nullptr, nullptr, st));
-  else
-    rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k, c->T,
-                                    at<void>(ws, L.xperm), nullptr, nullptr, nullptr, st));
+  // dispatch: token rows in grouped order (scatter from T = 2048: skewed step
+  // -1.2%; the row gather below it: decode 5 us faster than the scatter)
+  rc = cuda_rc(launch_dispatch_rows(x, at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), c->T,
+                                    c->k, c->D, at<void>(ws, L.xperm), nullptr, st));
   if (rc) return rc;
   moe_gemm_args g{};
   g.op = MOE_OP_GATE_UP_SWIGLU;
@@ -875,8 +868,8 @@ int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int
   rc = cuda_rc(launch_permute(blob, cfg->T, cfg->k, cfg->E, at<int32_t>(ws, L.chunk), counts,
                               offsets, perm_pair, inv_row, at<int>(ws, 0), st));
   if (rc || !x) return rc;
-  return cuda_rc(launch_gather_rows(x, perm_pair, cfg->T * cfg->k, cfg->D, cfg->k, cfg->T, x_perm,
-                                    nullptr, nullptr, nullptr, st));
+  return cuda_rc(launch_dispatch_rows(x, perm_pair, inv_row, cfg->T, cfg->k, cfg->D, x_perm,
+                                      nullptr, st));
 }
 
 int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* counts,
