@@ -628,7 +628,8 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
   // dispatch: token rows in grouped order (scatter from T = 2048: skewed step
   // -1.2%; the row gather below it: decode 5 us faster than the scatter)
   rc = cuda_rc(launch_dispatch_rows(x, at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), c->T,
-                                    c->k, c->D, at<void>(ws, L.xperm), nullptr, st));
+                                    c->k, c->D, at<void>(ws, L.xperm), nullptr, nullptr, nullptr,
+                                    st));
   if (rc) return rc;
   moe_gemm_args g{};
   g.op = MOE_OP_GATE_UP_SWIGLU;
@@ -755,8 +756,9 @@ int forward_experts_impl(const moe_config* c, const DevInfo& dev, const void* x,
   // grouped rows of the local experts: [offsets[e0], offsets[e1])
   const int32_t* row_lo = offsets + e0;
   const int32_t* row_hi = offsets + e1;
-  rc = cuda_rc(launch_gather_rows(x, at<int32_t>(ws, L.perm), c->T * c->k, c->D, c->k, c->T,
-                                  at<void>(ws, L.xperm), row_lo, row_hi, nullptr, st));
+  rc = cuda_rc(launch_dispatch_rows(x, at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), c->T,
+                                    c->k, c->D, at<void>(ws, L.xperm), row_lo, row_hi, nullptr,
+                                    st));
   if (rc) return rc;
   const int ts = s1 - s0;
   const void* x_sh = static_cast<const char*>(x) + static_cast<size_t>(s0) * c->D * 2;
@@ -869,7 +871,7 @@ int moe_permute(const moe_config* cfg, const int32_t* blob, int32_t* counts, int
                               offsets, perm_pair, inv_row, at<int>(ws, 0), st));
   if (rc || !x) return rc;
   return cuda_rc(launch_dispatch_rows(x, perm_pair, inv_row, cfg->T, cfg->k, cfg->D, x_perm,
-                                      nullptr, st));
+                                      nullptr, nullptr, nullptr, st));
 }
 
 int moe_permute_static(const moe_config* cfg, const int32_t* blob, int32_t* counts,

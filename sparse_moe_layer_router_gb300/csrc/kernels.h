@@ -70,13 +70,15 @@ cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int 
 cudaError_t launch_scatter_rows(const void* x, const int32_t* inv_row, int T, int k, int D,
                                 int rows, void* out, const int32_t* row_lo,
                                 const int32_t* row_hi, int* status, cudaStream_t st);
-// x rows in grouped order, x_perm[r] = x[perm_pair[r] / k]: from T =
-// kScatterMinTokens the token-major scatter (each x row read once; at large T
-// the grouped rows would evict x from L2 between a gather's k reads of a
-// row), below it the row gather (more blocks for small batches).
+// x rows in grouped order, x_perm[r] = x[perm_pair[r] / k] (with row_lo /
+// row_hi only for *row_lo <= r < *row_hi): from T = kScatterMinTokens the
+// token-major scatter (each x row read once; at large T the grouped rows
+// would evict x from L2 between a gather's k reads of a row), below it the
+// row gather (more blocks for small batches).
 constexpr int kScatterMinTokens = 2048;
 cudaError_t launch_dispatch_rows(const void* x, const int32_t* perm_pair, const int32_t* inv_row,
-                                 int T, int k, int D, void* x_perm, int* status, cudaStream_t st);
+                                 int T, int k, int D, void* x_perm, const int32_t* row_lo,
+                                 const int32_t* row_hi, int* status, cudaStream_t st);
 // Caller index arrays made safe for the grouped GEMM: offsets_out[i] = the
 // running maximum of offsets[0..i] clamped into [0, rows] (monotone, so every
 // group's row range lies inside [0, rows)); perm_out[r] = perm_pair[r] clamped

@@ -431,10 +431,11 @@ cudaError_t launch_scatter_rows(const void* x, const int32_t* inv_row, int T, in
 }
 
 cudaError_t launch_dispatch_rows(const void* x, const int32_t* perm_pair, const int32_t* inv_row,
-                                 int T, int k, int D, void* x_perm, int* status, cudaStream_t st) {
+                                 int T, int k, int D, void* x_perm, const int32_t* row_lo,
+                                 const int32_t* row_hi, int* status, cudaStream_t st) {
   if (T >= kScatterMinTokens)
-    return launch_scatter_rows(x, inv_row, T, k, D, T * k, x_perm, nullptr, nullptr, status, st);
-  return launch_gather_rows(x, perm_pair, T * k, D, k, T, x_perm, nullptr, nullptr, status, st);
+    return launch_scatter_rows(x, inv_row, T, k, D, T * k, x_perm, row_lo, row_hi, status, st);
+  return launch_gather_rows(x, perm_pair, T * k, D, k, T, x_perm, row_lo, row_hi, status, st);
 }
 
 cudaError_t launch_gather_rows(const void* a, const int32_t* idx, int rows, int D, int div,
@@ -547,7 +548,8 @@ cudaError_t launch_permute_static(const int32_t* blob, int T, int k, int E, int3
   if (e != cudaSuccess) return e;
   e = launch_permute(blob, T, k, E, table, counts, offsets, perm_pair, inv_row, nullptr, st);
   if (e != cudaSuccess || !x) return e;
-  return launch_dispatch_rows(x, perm_pair, inv_row, T, k, D, x_perm, nullptr, st);
+  return launch_dispatch_rows(x, perm_pair, inv_row, T, k, D, x_perm, nullptr, nullptr, nullptr,
+                              st);
 }
 
 }  // namespace moe
