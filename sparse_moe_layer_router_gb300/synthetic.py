@@ -65,6 +65,9 @@ CONFIGS = {
     # Same per-expert shapes as "decode" with 64 experts (1.6 GB of weights): the
     # case the detailed hardware-counter captures run on.
     "decode_e64": MoEConfig("decode_e64", T=64, D=4096, E=64, I=1024, Is=1024, k=10),
+    # bf16 with ~20 token rows per expert (as in the T=1024 prefill) on 64 experts
+    # (1.6 GB of weights): the hardware-counter capture case of the prefill shape.
+    "prefill_e64": MoEConfig("prefill_e64", T=128, D=4096, E=64, I=1024, Is=1024, k=10),
     # W4A16 with ~20 token rows per expert (as in the T=1024 prefill) on 64 experts
     # (0.42 GB of packed weights): the W4A16 hardware-counter capture case.
     "w4a16_e64": MoEConfig("w4a16_e64", T=128, D=4096, E=64, I=1024, Is=1024, k=10, quant=1),
