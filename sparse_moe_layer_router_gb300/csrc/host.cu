@@ -666,9 +666,10 @@ int forward_impl(const moe_config* c, const DevInfo& dev, const void* x, const m
 // moe_forward_host's first step: x copied into the workspace and routed.  From
 // T = 4096 the copy runs in chunks of 2048 tokens on the library's second
 // stream, and each chunk is routed on `st` once it has arrived (with the whole
-// batch's router plan), overlapping the copy of the chunks after it: the copy
-// is bound by the host link, and a 2048-token route call costs little more
-// per token than a whole batch's.
+// batch's router plan), overlapping the copy of the chunks after it.  The copy
+// is bound by the host link; a route call costs more per token on fewer
+// tokens (53 us for 1024, 165 us for 8192), and 2048-token chunks keep that
+// extra cost below what the overlap saves.
 int host_copy_and_route(const moe_config* c, const void* x_host, void* xd, const moe_weights* w,
                         void* ws, const Layout& L, cudaStream_t st) {
   const size_t row = static_cast<size_t>(c->D) * 2;
