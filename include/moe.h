@@ -224,8 +224,9 @@ int moe_router_logits(const moe_config *cfg, const void *x, const void *w_router
  *   perm_pair int32 [T*k]: grouped row r holds pair perm_pair[r],
  *   inv_row int32 [T*k]:   pair p sits in grouped row inv_row[p].
  * If x (bf16 [T][D]) and x_perm (bf16 [T*k][D]) are both non-NULL, the token
- * rows are also gathered in grouped order: x_perm[r] = x[perm_pair[r] / k].
- * Bit-exact and deterministic.  Expert ids outside [0, E) are undefined input.
+ * rows are also copied in grouped order: x_perm[r] = x[perm_pair[r] / k].
+ * Bit-exact and deterministic.  Expert ids outside [0, E) are clamped into it
+ * and recorded as MOE_ERR_INVALID_ARG in the status word of ws.
  */
 int moe_permute(const moe_config *cfg, const int32_t *blob, int32_t *counts,
                 int32_t *offsets, int32_t *perm_pair, int32_t *inv_row,
@@ -333,7 +334,8 @@ int moe_forward_host(const moe_config *cfg, const void *x_host,
  *   0 <= e_begin < e_end <= E; 0 <= shared_begin <= shared_end <= T.
  *   ws sized for MOE_ENTRY_FORWARD_EXPERTS.
  * Errors: MOE_ERR_INVALID_ARG for a bad range or a missing pointer; otherwise
- * as moe_forward.  Expert ids in the blob outside [0, E) are undefined input.
+ * as moe_forward.  Expert ids in the blob outside [0, E) are clamped into it
+ * and recorded as MOE_ERR_INVALID_ARG in the status word of ws.
  */
 int moe_forward_experts(const moe_config *cfg, const void *x, const int32_t *blob,
                         const moe_weights *w, int e_begin, int e_end, int shared_begin,
@@ -383,8 +385,9 @@ int moe_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned int limit_ms,
 
 /*
  * Releases what the library keeps between calls for the calling host thread
- * in the current CUDA context: the second stream and the two events of split
- * grouped GEMMs (see the conventions above).  Work already queued on them
+ * in the current CUDA context: the second stream and the two events that
+ * split grouped GEMMs and moe_forward_host's chunked copies use (see the
+ * conventions above).  Work already queued on them
  * still completes (the CUDA runtime defers the release), so the call is safe
  * with calls in flight.  The next split call creates them again.  Nothing
  * else is cached across calls except moe_permute_static's address of its
